@@ -1,0 +1,198 @@
+"""Thin Python binding of libswiglu_mlp.so (include/swiglu_mlp.h).
+
+Argument marshalling only: torch supplies device memory (``data_ptr()``) and
+the current CUDA stream; every step of the MLP runs in the library's CUDA
+kernels.  If the library is missing this module raises -- there is no
+fallback path.
+
+The three calls keep the C ABI's names:
+
+* ``swiglu_mlp_fwd(X, Wgu, Wd)``        -> (Y, saved)      saved = [G | U | A]
+* ``swiglu_mlp_fwd_nograd(X, Wgu, Wd)`` -> (Y, A)
+* ``swiglu_mlp_bwd(dY, X, Wgu, Wd, saved)`` -> (dX, dWgu, dWd); consumes saved
+
+Outputs may be passed in (``out=`` dicts) to avoid allocation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libswiglu_mlp.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "swiglu_mlp.h")
+
+SWIGLU_BF16, SWIGLU_F16, SWIGLU_F32_IEEE = 0, 1, 2
+SWIGLU_OP_FWD, SWIGLU_OP_FWD_NOGRAD, SWIGLU_OP_BWD = 0, 1, 2
+STATUS = {0: "SWIGLU_OK", 1: "SWIGLU_ERR_INVALID_ARG", 2: "SWIGLU_ERR_ALIGNMENT",
+          3: "SWIGLU_ERR_UNSUPPORTED", 4: "SWIGLU_ERR_WORKSPACE", 5: "SWIGLU_ERR_CUDA",
+          6: "SWIGLU_ERR_DEVICE_TIMEOUT"}
+
+_DT = {torch.bfloat16: SWIGLU_BF16, torch.float16: SWIGLU_F16, torch.float32: SWIGLU_F32_IEEE}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SwigluError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s (%s)" % (where, STATUS.get(code, code), status_string(code)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libswiglu_mlp.so is not built (run __graft_entry__.build() or "
+                              "python -m backward_tcgen05_tma_gb300.build); no fallback exists")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, ci, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        L.swiglu_mlp_element_bytes.restype = sz
+        L.swiglu_mlp_element_bytes.argtypes = [ci]
+        L.swiglu_mlp_saved_bytes.restype = sz
+        L.swiglu_mlp_saved_bytes.argtypes = [i64, i64, ci]
+        L.swiglu_mlp_workspace_bytes.restype = sz
+        L.swiglu_mlp_workspace_bytes.argtypes = [i64, i64, i64, ci, ci]
+        L.swiglu_mlp_fwd.restype = ci
+        L.swiglu_mlp_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
+        L.swiglu_mlp_fwd_nograd.restype = ci
+        L.swiglu_mlp_fwd_nograd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
+        L.swiglu_mlp_bwd.restype = ci
+        L.swiglu_mlp_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
+        L.swiglu_mlp_query_error.restype = ci
+        L.swiglu_mlp_query_error.argtypes = [vp, vp]
+        L.swiglu_status_string.restype = ctypes.c_char_p
+        L.swiglu_status_string.argtypes = [ci]
+        L.swiglu_mlp_set_wait_limit_ns.restype = ctypes.c_uint64
+        L.swiglu_mlp_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        L.swiglu_mlp_inject_stall_once.restype = None
+        L.swiglu_mlp_inject_stall_once.argtypes = [ci]
+        L.swiglu_mlp_last_launch_count.restype = ci
+        L.swiglu_mlp_last_launch_count.argtypes = []
+        _lib = L
+        return L
+
+
+def declared_symbols() -> list[str]:
+    """Function names declared in include/swiglu_mlp.h."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(swiglu_(?:mlp|status)_\w+)\s*\(", text)))
+
+
+def status_string(code: int) -> str:
+    return lib().swiglu_status_string(code).decode()
+
+
+def dtype_code(dtype: torch.dtype) -> int:
+    if dtype not in _DT:
+        raise TypeError("unsupported dtype %s (bf16, fp16 or fp32)" % dtype)
+    return _DT[dtype]
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise SwigluError(code, where)
+
+
+def workspace(M: int, D: int, H: int, dtype: torch.dtype, op: int, device) -> torch.Tensor:
+    n = lib().swiglu_mlp_workspace_bytes(M, D, H, dtype_code(dtype), op)
+    return torch.zeros(int(n), dtype=torch.uint8, device=device)
+
+
+def _dims(X, Wgu, Wd):
+    M, D = X.shape
+    H = Wgu.shape[0] // 2
+    if Wgu.shape != (2 * H, D) or Wd.shape != (D, H):
+        raise ValueError("shape mismatch: X %s, Wgu %s, Wd %s" % (tuple(X.shape), tuple(Wgu.shape),
+                                                                   tuple(Wd.shape)))
+    for t in (X, Wgu, Wd):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != X.dtype:
+            raise ValueError("inputs must be contiguous CUDA tensors of one dtype")
+    return M, D, H
+
+
+def swiglu_mlp_fwd(X, Wgu, Wd, out: dict | None = None, ws=None):
+    """Training forward: returns (Y [M,D], saved [M,3H])."""
+    M, D, H = _dims(X, Wgu, Wd)
+    out = out or {}
+    Y = out.get("Y")
+    Y = torch.empty(M, D, dtype=X.dtype, device=X.device) if Y is None else Y
+    saved = out.get("saved")
+    saved = torch.empty(M, 3 * H, dtype=X.dtype, device=X.device) if saved is None else saved
+    ws = workspace(M, D, H, X.dtype, SWIGLU_OP_FWD, X.device) if ws is None else ws
+    _check(lib().swiglu_mlp_fwd(_ptr(X), _ptr(Wgu), _ptr(Wd), _ptr(Y), _ptr(saved), M, D, H,
+                                dtype_code(X.dtype), _ptr(ws), ws.numel(), _stream(X.device)),
+           "swiglu_mlp_fwd")
+    return Y, saved
+
+
+def swiglu_mlp_fwd_nograd(X, Wgu, Wd, out: dict | None = None, ws=None):
+    """Inference forward: returns (Y [M,D], A [M,H]); G and U are never stored."""
+    M, D, H = _dims(X, Wgu, Wd)
+    out = out or {}
+    Y = out.get("Y")
+    Y = torch.empty(M, D, dtype=X.dtype, device=X.device) if Y is None else Y
+    A = out.get("A")
+    A = torch.empty(M, H, dtype=X.dtype, device=X.device) if A is None else A
+    ws = workspace(M, D, H, X.dtype, SWIGLU_OP_FWD_NOGRAD, X.device) if ws is None else ws
+    _check(lib().swiglu_mlp_fwd_nograd(_ptr(X), _ptr(Wgu), _ptr(Wd), _ptr(Y), _ptr(A), M, D, H,
+                                       dtype_code(X.dtype), _ptr(ws), ws.numel(),
+                                       _stream(X.device)),
+           "swiglu_mlp_fwd_nograd")
+    return Y, A
+
+
+def swiglu_mlp_bwd(dY, X, Wgu, Wd, saved, out: dict | None = None, ws=None):
+    """Backward: returns (dX [M,D], dWgu [2H,D], dWd [D,H]).  Overwrites the
+    G/U columns of ``saved`` with dG/dU (a second call on it is undefined)."""
+    M, D, H = _dims(X, Wgu, Wd)
+    if dY.shape != (M, D) or saved.shape != (M, 3 * H):
+        raise ValueError("dY/saved shape mismatch")
+    out = out or {}
+    dX = out.get("dX")
+    dX = torch.empty(M, D, dtype=X.dtype, device=X.device) if dX is None else dX
+    dWgu = out.get("dWgu")
+    dWgu = torch.empty(2 * H, D, dtype=X.dtype, device=X.device) if dWgu is None else dWgu
+    dWd = out.get("dWd")
+    dWd = torch.empty(D, H, dtype=X.dtype, device=X.device) if dWd is None else dWd
+    ws = workspace(M, D, H, X.dtype, SWIGLU_OP_BWD, X.device) if ws is None else ws
+    _check(lib().swiglu_mlp_bwd(_ptr(dY), _ptr(X), _ptr(Wgu), _ptr(Wd), _ptr(saved), _ptr(dX),
+                                _ptr(dWgu), _ptr(dWd), M, D, H, dtype_code(X.dtype), _ptr(ws),
+                                ws.numel(), _stream(X.device)),
+           "swiglu_mlp_bwd")
+    return dX, dWgu, dWd
+
+
+def swiglu_mlp_query_error(ws) -> int:
+    """Synchronises the current stream and returns the device error status."""
+    return int(lib().swiglu_mlp_query_error(_ptr(ws), _stream(ws.device)))
+
+
+def swiglu_mlp_set_wait_limit_ns(ns: int) -> int:
+    return int(lib().swiglu_mlp_set_wait_limit_ns(int(ns)))
+
+
+def swiglu_mlp_inject_stall_once(on: bool = True) -> None:
+    lib().swiglu_mlp_inject_stall_once(1 if on else 0)
+
+
+def swiglu_mlp_last_launch_count() -> int:
+    return int(lib().swiglu_mlp_last_launch_count())

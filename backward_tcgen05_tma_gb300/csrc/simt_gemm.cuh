@@ -1,0 +1,122 @@
+// simt_gemm.cuh -- true-IEEE fp32 path: shared-memory-tiled FFMA GEMMs on
+// the CUDA cores with the MLP's fused epilogues.  No tensor core, so no TF32:
+// "[RFC] Testing Methodology for FP32 Convergence Tests on Fused
+// SwiGLU/dSwiGLU Kernels" (Liger-Kernel #1383), "Root Cause" traces the fp32
+// failures to TF32 matmuls, and "Approaches I tried" to the software-FMA
+// path's shared-memory appetite on SM120 (a 64x64x16 fp32 tile pair here needs
+// 8.5 KB, far inside sm_103a's 227 KB).
+//
+//   C[m, n] = sum_k A(m, k) B(n, k),  A(m, k) = A[m * sam + k * sak],
+//                                     B(n, k) = B[n * sbn + k * sbk]
+// Arbitrary element strides cover every K-major / MN-major operand of the
+// six GEMMs.  A 64 x 64 output tile per 256-thread block, 4 x 4 per thread.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace swiglu {
+
+constexpr int SG_BM = 64, SG_BN = 64, SG_BK = 16, SG_THREADS = 256;
+
+struct SimtOperand {
+  const float* p;
+  int64_t s_row;  // stride of the output-row index (m for A, n for B)
+  int64_t s_k;    // stride of the contraction index
+};
+
+// Plain store: out[m * ld + n] = acc.
+struct SimtEpiStore {
+  float* out;
+  int64_t ld;
+  __device__ __forceinline__ void apply(int m, int n, float acc, float) const {
+    out[(int64_t)m * ld + n] = acc;
+  }
+};
+
+// Gate/up: acc = g, acc2 = u for hidden unit n.  Stores G, U (if g != null)
+// and A = SiLU(g) * u, SiLU(g) = g / (1 + e^-g) with IEEE expf and division.
+struct SimtEpiSwiGLU {
+  float* g;
+  float* u;
+  int64_t ld_gu;
+  float* a;
+  int64_t ld_a;
+  __device__ __forceinline__ void apply(int m, int n, float gv, float uv) const {
+    if (g != nullptr) {
+      g[(int64_t)m * ld_gu + n] = gv;
+      u[(int64_t)m * ld_gu + n] = uv;
+    }
+    a[(int64_t)m * ld_a + n] = gv / (1.0f + expf(-gv)) * uv;
+  }
+};
+
+// Backward: acc = dA for hidden unit n; reads the stored G, U and overwrites
+// them with dG = dA * U * SiLU'(G), dU = dA * SiLU(G).
+struct SimtEpiDSwiGLU {
+  float* g;
+  float* u;
+  int64_t ld;
+  __device__ __forceinline__ void apply(int m, int n, float da, float) const {
+    const int64_t o = (int64_t)m * ld + n;
+    const float gv = g[o], uv = u[o];
+    const float s = 1.0f / (1.0f + expf(-gv));
+    u[o] = da * (gv * s);
+    g[o] = da * uv * (s * (1.0f + gv * (1.0f - s)));
+  }
+};
+
+// DUAL: a second B operand (B2) accumulated alongside B; the epilogue gets
+// both sums (used by the gate/up GEMM: B = Wg rows, B2 = Wu rows).
+template <bool DUAL, class Epi>
+__global__ void __launch_bounds__(SG_THREADS)
+    simt_gemm_kernel(SimtOperand A, SimtOperand B, SimtOperand B2, int M, int N, int K, Epi epi) {
+  __shared__ float As[SG_BK][SG_BM + 4];
+  __shared__ float Bs[SG_BK][SG_BN + 4];
+  __shared__ float B2s[DUAL ? SG_BK : 1][SG_BN + 4];
+
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.y * SG_BM, n0 = blockIdx.x * SG_BN;
+  float acc[4][4] = {}, acc2[4][4] = {};
+
+  for (int k0 = 0; k0 < K; k0 += SG_BK) {
+#pragma unroll
+    for (int i = 0; i < (SG_BM * SG_BK) / SG_THREADS; ++i) {
+      const int idx = threadIdx.x + i * SG_THREADS;
+      const int r = idx / SG_BK, kk = idx % SG_BK;
+      const int m = m0 + r, n = n0 + r, k = k0 + kk;
+      As[kk][r] = (m < M && k < K) ? A.p[(int64_t)m * A.s_row + (int64_t)k * A.s_k] : 0.0f;
+      Bs[kk][r] = (n < N && k < K) ? B.p[(int64_t)n * B.s_row + (int64_t)k * B.s_k] : 0.0f;
+      if (DUAL)
+        B2s[kk][r] = (n < N && k < K) ? B2.p[(int64_t)n * B2.s_row + (int64_t)k * B2.s_k] : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < SG_BK; ++kk) {
+      float a[4], b[4], b2[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i] = As[kk][ty * 4 + i];
+        b[i] = Bs[kk][tx * 4 + i];
+        if (DUAL) b2[i] = B2s[kk][tx * 4 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+          if (DUAL) acc2[i][j] = fmaf(a[i], b2[j], acc2[i][j]);
+        }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int m = m0 + ty * 4 + i, n = n0 + tx * 4 + j;
+      if (m < M && n < N) epi.apply(m, n, acc[i][j], acc2[i][j]);
+    }
+}
+
+}  // namespace swiglu

@@ -1,0 +1,425 @@
+// swiglu_mlp.cu -- C ABI of the fused SwiGLU MLP (include/swiglu_mlp.h):
+// argument validation, TMA tensor-map encoding and kernel launches.
+//
+// Forward ("[RFC] Full-pipeline SwiGLU MLP with forward/backward
+// co-optimization", Liger-Kernel #1347, "Summary"):
+//   gate/up   [G | U | A] = X [Wg; Wu]^T with the SwiGLU epilogue
+//   down      Y = A Wd^T
+// Backward:
+//   dGU       dA = dY Wd in TMEM only; epilogue writes dG, dU over G, U
+//   dWd       dWd = dY^T A
+//   dWgu      [dWg; dWu] = [dG | dU]^T X            (one GEMM)
+//   dX        dX = [dG | dU] [Wg; Wu], K = 2H       (one accumulator)
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/swiglu_mlp.h"
+#include "simt_gemm.cuh"
+#include "tc_gemm.cuh"
+
+using namespace swiglu;
+
+namespace {
+
+constexpr size_t WS_HEADER = 256;  // error word + reserved
+constexpr int TC_STAGES = 4;
+constexpr int TC_BN = 256;
+
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_inject_stall{0};
+std::atomic<int> g_last_launches{0};
+
+// ---------------------------------------------------------------------------
+// driver entry point for tensor-map encoding (no link-time libcuda dependency)
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// 2-D tiled map over a row-major matrix [outer][inner] (inner contiguous) with
+// a row stride in bytes; 128-byte swizzle; out-of-range elements read as 0.
+bool encode_2d(CUtensorMap* tm, bool bf16, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Wgu [2H][D] seen as [2][H][D]: one box brings rows j0.. of Wg and of Wu.
+bool encode_gateup(CUtensorMap* tm, bool bf16, const void* Wgu, uint64_t D, uint64_t H,
+                   uint32_t rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {D, H, 2};
+  cuuint64_t strides[2] = {D * 2, H * D * 2};
+  cuuint32_t box[3] = {64, rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+             const_cast<void*>(Wgu), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// K-major operand: rows of K elements, box {64, rows_per_tile}.
+bool map_kmajor(CUtensorMap* tm, bool bf16, const void* base, int64_t K, int64_t rows, int64_t ld,
+                uint32_t box_rows) {
+  return encode_2d(tm, bf16, base, (uint64_t)K, (uint64_t)rows, (uint64_t)ld * 2, 64, box_rows);
+}
+
+// MN-major operand stored [K][MN]: boxes {64 MN, 64 K}.
+bool map_mnmajor(CUtensorMap* tm, bool bf16, const void* base, int64_t MN, int64_t K, int64_t ld) {
+  return encode_2d(tm, bf16, base, (uint64_t)MN, (uint64_t)K, (uint64_t)ld * 2, 64, 64);
+}
+
+TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err) {
+  TcShape s;
+  s.M = (int)M;
+  s.N = (int)N;
+  s.K = (int)K;
+  s.m_tiles = (int)((M + TC_BM - 1) / TC_BM);
+  s.n_tiles = (int)((N + n_per_tile - 1) / n_per_tile);
+  s.k_blocks = (int)((K + TC_BK - 1) / TC_BK);
+  s.group_m = 16;
+  s.wait_limit_ns = g_wait_limit_ns.load();
+  s.err = err;
+  s.inject_stall = g_inject_stall.exchange(0);
+  return s;
+}
+
+template <int AM, int BMODE, bool BF16, class Epi>
+cudaError_t launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const TcShape& s,
+                      const typename Epi::Params& ep, cudaStream_t st) {
+  auto kern = tc_gemm_kernel<TC_BN, TC_STAGES, AM, BMODE, BF16, Epi>;
+  constexpr int smem = TcSmem<TC_BN, TC_STAGES>::DYN_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int tiles = s.m_tiles * s.n_tiles;
+  const int nsm = sm_count();
+  const int grid = tiles < nsm ? tiles : nsm;
+  kern<<<grid, TC_THREADS, smem, st>>>(ta, tb, s, ep);
+  g_last_launches.fetch_add(1);
+  return cudaGetLastError();
+}
+
+template <bool DUAL, class Epi>
+cudaError_t launch_simt(SimtOperand A, SimtOperand B, SimtOperand B2, int64_t M, int64_t N,
+                        int64_t K, const Epi& epi, cudaStream_t st) {
+  dim3 grid((unsigned)((N + SG_BN - 1) / SG_BN), (unsigned)((M + SG_BM - 1) / SG_BM));
+  simt_gemm_kernel<DUAL, Epi><<<grid, SG_THREADS, 0, st>>>(A, B, B2, (int)M, (int)N, (int)K, epi);
+  g_last_launches.fetch_add(1);
+  return cudaGetLastError();
+}
+
+size_t elt_bytes(swiglu_dtype dt) {
+  switch (dt) {
+    case SWIGLU_BF16:
+    case SWIGLU_F16: return 2;
+    case SWIGLU_F32_IEEE: return 4;
+    default: return 0;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape/dtype/workspace checks shared by every entry point.  Pointers are
+// checked by the callers (which know which ones they use).
+swiglu_status check_common(int64_t M, int64_t D, int64_t H, swiglu_dtype dt, const void* ws,
+                           size_t ws_bytes, int op) {
+  if (elt_bytes(dt) == 0) return SWIGLU_ERR_INVALID_ARG;
+  if (M < 0 || D <= 0 || H <= 0) return SWIGLU_ERR_INVALID_ARG;
+  const int64_t mult = dt == SWIGLU_F32_IEEE ? 4 : 8;
+  if (D % mult != 0 || H % mult != 0) return SWIGLU_ERR_ALIGNMENT;
+  const int64_t lim = 0x7fffffffLL;
+  if (M > lim || D > lim || 3 * H > lim) return SWIGLU_ERR_UNSUPPORTED;
+  if (ws == nullptr || ws_bytes < swiglu_mlp_workspace_bytes(M, D, H, dt, op))
+    return SWIGLU_ERR_WORKSPACE;
+  if (!aligned16(ws)) return SWIGLU_ERR_ALIGNMENT;
+  return SWIGLU_OK;
+}
+
+swiglu_status check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p == nullptr) return SWIGLU_ERR_INVALID_ARG;
+  for (const void* p : ps)
+    if (!aligned16(p)) return SWIGLU_ERR_ALIGNMENT;
+  return SWIGLU_OK;
+}
+
+swiglu_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA; }
+
+// ---------------------------------------------------------------------------
+// tensor-core (bf16 / fp16) paths
+// ---------------------------------------------------------------------------
+template <bool BF16>
+swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y, void* G,
+                         void* U, int64_t ld_gu, void* A, int64_t ld_a, int64_t M, int64_t D,
+                         int64_t H, int* err, cudaStream_t st) {
+  CUtensorMap tx, tw, ta, twd;
+  // gate/up + SwiGLU: C[m, j | H + j], N counts hidden units, BN/2 per tile
+  if (!map_kmajor(&tx, BF16, X, D, M, D, TC_BM) || !encode_gateup(&tw, BF16, Wgu, D, H, TC_BN / 2))
+    return SWIGLU_ERR_CUDA;
+  TcShape s1 = make_shape(M, H, D, TC_BN / 2, err);
+  EpiSwiGLU::Params p1{G, U, ld_gu, A, ld_a};
+  cudaError_t e = launch_tc<LOAD_KMAJOR, LOAD_GATEUP, BF16, EpiSwiGLU>(tx, tw, s1, p1, st);
+  if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
+  // down projection: Y = A Wd^T
+  if (!map_kmajor(&ta, BF16, A, H, M, ld_a, TC_BM) || !map_kmajor(&twd, BF16, Wd, H, D, H, TC_BN))
+    return SWIGLU_ERR_CUDA;
+  TcShape s2 = make_shape(M, D, H, TC_BN, err);
+  EpiStore::Params p2{Y, D};
+  return cuda_status(launch_tc<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore>(ta, twd, s2, p2, st));
+}
+
+template <bool BF16>
+swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const void* Wd,
+                          void* saved, void* dX, void* dWgu, void* dWd, int64_t M, int64_t D,
+                          int64_t H, int* err, cudaStream_t st) {
+  const int64_t ld = 3 * H;
+  char* sv = static_cast<char*>(saved);
+  void* G = sv;
+  void* U = sv + H * 2;
+  void* A = sv + 2 * H * 2;
+  CUtensorMap m1, m2;
+  cudaError_t e;
+  // dA = dY Wd (Wd read MN-major as [K = D][N = H]); dG, dU in place
+  if (!map_kmajor(&m1, BF16, dY, D, M, D, TC_BM) || !map_mnmajor(&m2, BF16, Wd, H, D, H))
+    return SWIGLU_ERR_CUDA;
+  {
+    TcShape s = make_shape(M, H, D, TC_BN, err);
+    EpiDSwiGLU::Params p{G, U, ld};
+    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLU>(m1, m2, s, p, st);
+    if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
+  }
+  // dWd [D, H] = dY^T A: both operands MN-major over the token dimension
+  if (!map_mnmajor(&m1, BF16, dY, D, M, D) || !map_mnmajor(&m2, BF16, A, H, M, ld))
+    return SWIGLU_ERR_CUDA;
+  {
+    TcShape s = make_shape(D, H, M, TC_BN, err);
+    EpiStore::Params p{dWd, H};
+    e = launch_tc<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(m1, m2, s, p, st);
+    if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
+  }
+  // [dWg; dWu] [2H, D] = [dG | dU]^T X: one GEMM over the 2H columns
+  if (!map_mnmajor(&m1, BF16, G, 2 * H, M, ld) || !map_mnmajor(&m2, BF16, X, D, M, D))
+    return SWIGLU_ERR_CUDA;
+  {
+    TcShape s = make_shape(2 * H, D, M, TC_BN, err);
+    EpiStore::Params p{dWgu, D};
+    e = launch_tc<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(m1, m2, s, p, st);
+    if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
+  }
+  // dX [M, D] = [dG | dU] [Wg; Wu]: K = 2H in one accumulator
+  if (!map_kmajor(&m1, BF16, G, 2 * H, M, ld, TC_BM) || !map_mnmajor(&m2, BF16, Wgu, D, 2 * H, D))
+    return SWIGLU_ERR_CUDA;
+  {
+    TcShape s = make_shape(M, D, 2 * H, TC_BN, err);
+    EpiStore::Params p{dX, D};
+    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(m1, m2, s, p, st);
+    if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
+  }
+  return SWIGLU_OK;
+}
+
+// ---------------------------------------------------------------------------
+// fp32 IEEE (CUDA-core FFMA) paths
+// ---------------------------------------------------------------------------
+swiglu_status simt_forward(const float* X, const float* Wgu, const float* Wd, float* Y, float* G,
+                           float* U, int64_t ld_gu, float* A, int64_t ld_a, int64_t M, int64_t D,
+                           int64_t H, cudaStream_t st) {
+  SimtOperand x{X, D, 1}, wg{Wgu, D, 1}, wu{Wgu + H * D, D, 1};
+  cudaError_t e = launch_simt<true>(x, wg, wu, M, H, D, SimtEpiSwiGLU{G, U, ld_gu, A, ld_a}, st);
+  if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
+  SimtOperand a{A, ld_a, 1}, wd{Wd, H, 1};
+  return cuda_status(launch_simt<false>(a, wd, wd, M, D, H, SimtEpiStore{Y, D}, st));
+}
+
+swiglu_status simt_backward(const float* dY, const float* X, const float* Wgu, const float* Wd,
+                            float* saved, float* dX, float* dWgu, float* dWd, int64_t M,
+                            int64_t D, int64_t H, cudaStream_t st) {
+  const int64_t ld = 3 * H;
+  float* G = saved;
+  float* U = saved + H;
+  float* A = saved + 2 * H;
+  cudaError_t e;
+  // dA = dY Wd: A(m, d) = dY[m, d]; B(j, d) = Wd[d, j]
+  e = launch_simt<false>(SimtOperand{dY, D, 1}, SimtOperand{Wd, 1, H}, SimtOperand{Wd, 1, H}, M,
+                         H, D, SimtEpiDSwiGLU{G, U, ld}, st);
+  if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
+  // dWd[d, j] = sum_m dY[m, d] A[m, j]
+  e = launch_simt<false>(SimtOperand{dY, 1, D}, SimtOperand{A, 1, ld}, SimtOperand{A, 1, ld}, D,
+                         H, M, SimtEpiStore{dWd, H}, st);
+  if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
+  // dWgu[j', d] = sum_m dGU[m, j'] X[m, d]
+  e = launch_simt<false>(SimtOperand{G, 1, ld}, SimtOperand{X, 1, D}, SimtOperand{X, 1, D}, 2 * H,
+                         D, M, SimtEpiStore{dWgu, D}, st);
+  if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
+  // dX[m, d] = sum_j' dGU[m, j'] Wgu[j', d]
+  e = launch_simt<false>(SimtOperand{G, ld, 1}, SimtOperand{Wgu, 1, D}, SimtOperand{Wgu, 1, D}, M,
+                         D, 2 * H, SimtEpiStore{dX, D}, st);
+  return cuda_status(e);
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+size_t swiglu_mlp_element_bytes(swiglu_dtype dtype) { return elt_bytes(dtype); }
+
+size_t swiglu_mlp_saved_bytes(int64_t M, int64_t H, swiglu_dtype dtype) {
+  if (M < 0 || H < 0) return 0;
+  return (size_t)M * (size_t)(3 * H) * elt_bytes(dtype);
+}
+
+size_t swiglu_mlp_workspace_bytes(int64_t M, int64_t D, int64_t H, swiglu_dtype dtype, int op) {
+  (void)M;
+  (void)D;
+  (void)H;
+  (void)dtype;
+  (void)op;
+  return WS_HEADER;
+}
+
+swiglu_status swiglu_mlp_fwd(const void* X, const void* Wgu, const void* Wd, void* Y, void* saved,
+                             int64_t M, int64_t D, int64_t H, swiglu_dtype dtype, void* ws,
+                             size_t ws_bytes, void* stream) {
+  g_last_launches.store(0);
+  swiglu_status st = check_common(M, D, H, dtype, ws, ws_bytes, SWIGLU_OP_FWD);
+  if (st != SWIGLU_OK) return st;
+  if (M == 0) return SWIGLU_OK;
+  if ((st = check_ptrs({X, Wgu, Wd, Y, saved})) != SWIGLU_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = static_cast<int*>(ws);
+  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
+  const size_t e = elt_bytes(dtype);
+  char* sv = static_cast<char*>(saved);
+  void* G = sv;
+  void* U = sv + H * e;
+  void* A = sv + 2 * H * e;
+  switch (dtype) {
+    case SWIGLU_BF16:
+      return tc_forward<true>(X, Wgu, Wd, Y, G, U, 3 * H, A, 3 * H, M, D, H, err, s);
+    case SWIGLU_F16:
+      return tc_forward<false>(X, Wgu, Wd, Y, G, U, 3 * H, A, 3 * H, M, D, H, err, s);
+    default:
+      return simt_forward((const float*)X, (const float*)Wgu, (const float*)Wd, (float*)Y,
+                          (float*)G, (float*)U, 3 * H, (float*)A, 3 * H, M, D, H, s);
+  }
+}
+
+swiglu_status swiglu_mlp_fwd_nograd(const void* X, const void* Wgu, const void* Wd, void* Y,
+                                    void* A, int64_t M, int64_t D, int64_t H, swiglu_dtype dtype,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  g_last_launches.store(0);
+  swiglu_status st = check_common(M, D, H, dtype, ws, ws_bytes, SWIGLU_OP_FWD_NOGRAD);
+  if (st != SWIGLU_OK) return st;
+  if (M == 0) return SWIGLU_OK;
+  if ((st = check_ptrs({X, Wgu, Wd, Y, A})) != SWIGLU_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = static_cast<int*>(ws);
+  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
+  switch (dtype) {
+    case SWIGLU_BF16:
+      return tc_forward<true>(X, Wgu, Wd, Y, nullptr, nullptr, 0, A, H, M, D, H, err, s);
+    case SWIGLU_F16:
+      return tc_forward<false>(X, Wgu, Wd, Y, nullptr, nullptr, 0, A, H, M, D, H, err, s);
+    default:
+      return simt_forward((const float*)X, (const float*)Wgu, (const float*)Wd, (float*)Y,
+                          nullptr, nullptr, 0, (float*)A, H, M, D, H, s);
+  }
+}
+
+swiglu_status swiglu_mlp_bwd(const void* dY, const void* X, const void* Wgu, const void* Wd,
+                             void* saved, void* dX, void* dWgu, void* dWd, int64_t M, int64_t D,
+                             int64_t H, swiglu_dtype dtype, void* ws, size_t ws_bytes,
+                             void* stream) {
+  g_last_launches.store(0);
+  swiglu_status st = check_common(M, D, H, dtype, ws, ws_bytes, SWIGLU_OP_BWD);
+  if (st != SWIGLU_OK) return st;
+  if (M == 0) return SWIGLU_OK;  // gradients of an empty batch: nothing is written
+  if ((st = check_ptrs({dY, X, Wgu, Wd, saved, dX, dWgu, dWd})) != SWIGLU_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = static_cast<int*>(ws);
+  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
+  switch (dtype) {
+    case SWIGLU_BF16:
+      return tc_backward<true>(dY, X, Wgu, Wd, saved, dX, dWgu, dWd, M, D, H, err, s);
+    case SWIGLU_F16:
+      return tc_backward<false>(dY, X, Wgu, Wd, saved, dX, dWgu, dWd, M, D, H, err, s);
+    default:
+      return simt_backward((const float*)dY, (const float*)X, (const float*)Wgu,
+                           (const float*)Wd, (float*)saved, (float*)dX, (float*)dWgu,
+                           (float*)dWd, M, D, H, s);
+  }
+}
+
+swiglu_status swiglu_mlp_query_error(const void* ws, void* stream) {
+  if (ws == nullptr) return SWIGLU_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int host = 0;
+  if (cudaMemcpyAsync(&host, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SWIGLU_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SWIGLU_ERR_CUDA;
+  if (host == DEV_ERR_TIMEOUT) return SWIGLU_ERR_DEVICE_TIMEOUT;
+  return host == 0 ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
+
+const char* swiglu_status_string(swiglu_status status) {
+  switch (status) {
+    case SWIGLU_OK: return "ok";
+    case SWIGLU_ERR_INVALID_ARG: return "invalid argument (null pointer, bad size or dtype)";
+    case SWIGLU_ERR_ALIGNMENT: return "misaligned pointer or D/H not a multiple of 8 (4 for fp32)";
+    case SWIGLU_ERR_UNSUPPORTED: return "shape outside the supported range";
+    case SWIGLU_ERR_WORKSPACE: return "workspace missing or too small";
+    case SWIGLU_ERR_CUDA: return "CUDA error";
+    case SWIGLU_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+uint64_t swiglu_mlp_set_wait_limit_ns(uint64_t ns) {
+  if (ns < 1000) ns = 1000;
+  return g_wait_limit_ns.exchange(ns);
+}
+
+void swiglu_mlp_inject_stall_once(int on) { g_inject_stall.store(on ? 1 : 0); }
+
+int swiglu_mlp_last_launch_count(void) { return g_last_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,466 @@
+// tc_gemm.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a with
+// the SwiGLU-MLP epilogues.
+//
+//   C[m, n] = sum_k A[m, k] * B[n, k]      (fp32 accumulation in TMEM)
+//
+// Each operand is read from global memory by TMA into 128-byte-swizzled
+// shared-memory tiles, either K-major (K contiguous in memory) or MN-major (M
+// or N contiguous); the tensor core reads both layouts natively, so no
+// operand of the MLP's six GEMMs is ever transposed in memory.
+//
+// CTA = 6 warps, one CTA per SM, persistent over output tiles:
+//   warp 0      TMA producer: fills a STAGES-deep ring of (A, B) k-blocks
+//   warp 1      owns TMEM (allocates 2 x BN columns) and issues tcgen05.mma
+//   warps 2..5  epilogue: TMEM -> registers -> fused elementwise -> global
+// Two TMEM accumulators alternate between tiles, so the epilogue of tile i
+// overlaps the main loop of tile i + 1.  Every wait is bounded (see
+// mbar_wait_bounded); a stuck pipeline records an error and the CTA unwinds.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "sm103_ptx.cuh"
+
+namespace swiglu {
+
+constexpr int TC_BM = 128;       // tile rows (MMA M)
+constexpr int TC_BK = 64;        // k-block: 64 16-bit elements = one 128-byte swizzle row
+constexpr int TC_THREADS = 192;  // 6 warps
+constexpr int TC_UMMA_K = 16;    // K of one kind::f16 MMA
+
+enum LoadMode : int {
+  LOAD_KMAJOR = 0,   // operand rows are contiguous along K: one box {64, rows}
+  LOAD_MNMAJOR = 1,  // operand is stored [K][MN]: boxes {64 MN, 64 K}, one per 64-wide chunk
+  LOAD_GATEUP = 2    // Wgu viewed as [2][H][D]: one 3-D box {64, rows/2, 2} = Wg rows then Wu rows
+};
+
+struct TcShape {
+  int M, N, K;           // GEMM problem (N counts hidden units for the gate/up GEMM)
+  int m_tiles, n_tiles;  // output tiles
+  int k_blocks;          // ceil(K / 64)
+  int group_m;           // rasterisation: m tiles per group
+  uint64_t wait_limit_ns;
+  int* err;              // device error word (workspace)
+  int inject_stall;      // test hook: producer skips stage 0 of its first tile
+};
+
+// Tile order: groups of group_m m-tiles, m fastest inside a group, so the CTAs
+// running at one time share a few A row-blocks and B column-blocks in L2.
+__device__ __forceinline__ void tc_tile_coords(int t, const TcShape& s, int& mt, int& nt) {
+  const int per_group = s.group_m * s.n_tiles;
+  const int g = t / per_group;
+  const int r = t - g * per_group;
+  const int gm0 = g * s.group_m;
+  const int gh = min(s.group_m, s.m_tiles - gm0);
+  mt = gm0 + r % gh;
+  nt = r / gh;
+}
+
+// ---------------------------------------------------------------------------
+// Epilogues.  Each is called by the 128 epilogue threads of a CTA for one
+// output tile; thread `row` (0..127) owns output row m0 + row and reads its
+// TMEM lane.  `tacc` is the TMEM address of this warp's lane quarter at the
+// accumulator's first column.
+// ---------------------------------------------------------------------------
+template <bool BF16>
+struct Pack;
+template <>
+struct Pack<true> {
+  using T = __nv_bfloat16;
+  static __device__ __forceinline__ uint32_t two(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ float2 unpack(uint32_t w) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
+    return __bfloat1622float2(h);
+  }
+};
+template <>
+struct Pack<false> {
+  using T = __half;
+  static __device__ __forceinline__ uint32_t two(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ float2 unpack(uint32_t w) {
+    __half2 h = *reinterpret_cast<__half2*>(&w);
+    return __half22float2(h);
+  }
+};
+
+// SiLU(g) = g / (1 + e^-g), evaluated in fp32.
+__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + __expf(-g)); }
+
+// Plain store: C[m, n] = rnd(acc).
+struct EpiStore {
+  struct Params {
+    void* out;
+    int64_t ld;  // elements
+  };
+  template <int BN, bool BF16>
+  static __device__ __forceinline__ void run(const Params& p, const TcShape& s, uint32_t tacc,
+                                             int m0, int nt, int row) {
+    using P = Pack<BF16>;
+    const int m = m0 + row;
+    const int n0 = nt * BN;
+    typename P::T* out = reinterpret_cast<typename P::T*>(p.out) + (int64_t)m * p.ld;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tacc + c * 32, r);
+      tmem_ld_wait();
+      if (m < s.M) {
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) {
+          const int n = n0 + c * 32 + g8 * 8;
+          if (n + 8 <= s.N) {
+            uint4 v;
+            v.x = P::two(__uint_as_float(r[g8 * 8 + 0]), __uint_as_float(r[g8 * 8 + 1]));
+            v.y = P::two(__uint_as_float(r[g8 * 8 + 2]), __uint_as_float(r[g8 * 8 + 3]));
+            v.z = P::two(__uint_as_float(r[g8 * 8 + 4]), __uint_as_float(r[g8 * 8 + 5]));
+            v.w = P::two(__uint_as_float(r[g8 * 8 + 6]), __uint_as_float(r[g8 * 8 + 7]));
+            *reinterpret_cast<uint4*>(out + n) = v;
+          }
+        }
+      }
+    }
+  }
+};
+
+// Gate/up epilogue: accumulator columns [0, BN/2) hold G for hidden units
+// j0 .. j0 + BN/2 - 1 and [BN/2, BN) hold U for the same units.  Stores
+// rnd(G), rnd(U) (training) and A = rnd(SiLU(G) * U) from the unrounded fp32
+// values.  With g == nullptr only A is written (no-grad).
+struct EpiSwiGLU {
+  struct Params {
+    void* g;       // G base ([M, ld_gu]); U at u
+    void* u;
+    int64_t ld_gu;
+    void* a;       // A base
+    int64_t ld_a;
+  };
+  template <int BN, bool BF16>
+  static __device__ __forceinline__ void run(const Params& p, const TcShape& s, uint32_t tacc,
+                                             int m0, int nt, int row) {
+    using P = Pack<BF16>;
+    using T = typename P::T;
+    constexpr int HALF = BN / 2;
+    const int m = m0 + row;
+    const int j0 = nt * HALF;
+    const bool keep_gu = p.g != nullptr;
+#pragma unroll 1
+    for (int c = 0; c < HALF / 32; ++c) {
+      uint32_t rg[32], ru[32];
+      tmem_ld_32x32b_x32(tacc + c * 32, rg);
+      tmem_ld_32x32b_x32(tacc + HALF + c * 32, ru);
+      tmem_ld_wait();
+      if (m < s.M) {
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) {
+          const int j = j0 + c * 32 + g8 * 8;
+          if (j + 8 <= s.N) {
+            uint4 va, vg, vu;
+            uint32_t* pa = &va.x;
+            uint32_t* pg = &vg.x;
+            uint32_t* pu = &vu.x;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float g0 = __uint_as_float(rg[g8 * 8 + 2 * e]);
+              const float g1 = __uint_as_float(rg[g8 * 8 + 2 * e + 1]);
+              const float u0 = __uint_as_float(ru[g8 * 8 + 2 * e]);
+              const float u1 = __uint_as_float(ru[g8 * 8 + 2 * e + 1]);
+              pa[e] = P::two(silu_f32(g0) * u0, silu_f32(g1) * u1);
+              pg[e] = P::two(g0, g1);
+              pu[e] = P::two(u0, u1);
+            }
+            *reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.a) + (int64_t)m * p.ld_a + j) = va;
+            if (keep_gu) {
+              *reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.g) + (int64_t)m * p.ld_gu + j) = vg;
+              *reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.u) + (int64_t)m * p.ld_gu + j) = vu;
+            }
+          }
+        }
+      }
+    }
+  }
+};
+
+// Backward SwiGLU epilogue: the accumulator is dA = dY Wd for hidden units
+// j0 .. j0 + BN - 1 (never stored).  Reads the stored G, U, writes
+//   dU = rnd(dA * SiLU(G)),  dG = rnd(dA * U * SiLU'(G))
+// over them in place, SiLU'(g) = s (1 + g (1 - s)), s = 1 / (1 + e^-g).
+struct EpiDSwiGLU {
+  struct Params {
+    void* g;  // G (becomes dG); U (becomes dU) at u
+    void* u;
+    int64_t ld;
+  };
+  template <int BN, bool BF16>
+  static __device__ __forceinline__ void run(const Params& p, const TcShape& s, uint32_t tacc,
+                                             int m0, int nt, int row) {
+    using P = Pack<BF16>;
+    using T = typename P::T;
+    const int m = m0 + row;
+    const int j0 = nt * BN;
+    T* grow = reinterpret_cast<T*>(p.g) + (int64_t)m * p.ld;
+    T* urow = reinterpret_cast<T*>(p.u) + (int64_t)m * p.ld;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tacc + c * 32, r);
+      tmem_ld_wait();
+      if (m < s.M) {
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) {
+          const int j = j0 + c * 32 + g8 * 8;
+          if (j + 8 <= s.N) {
+            const uint4 vg = *reinterpret_cast<const uint4*>(grow + j);
+            const uint4 vu = *reinterpret_cast<const uint4*>(urow + j);
+            const uint32_t* pg = &vg.x;
+            const uint32_t* pu = &vu.x;
+            uint4 og, ou;
+            uint32_t* qg = &og.x;
+            uint32_t* qu = &ou.x;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 g = P::unpack(pg[e]);
+              const float2 u = P::unpack(pu[e]);
+              const float da0 = __uint_as_float(r[g8 * 8 + 2 * e]);
+              const float da1 = __uint_as_float(r[g8 * 8 + 2 * e + 1]);
+              const float s0 = 1.0f / (1.0f + __expf(-g.x));
+              const float s1 = 1.0f / (1.0f + __expf(-g.y));
+              const float ds0 = s0 * (1.0f + g.x * (1.0f - s0));
+              const float ds1 = s1 * (1.0f + g.y * (1.0f - s1));
+              qu[e] = P::two(da0 * (g.x * s0), da1 * (g.y * s1));
+              qg[e] = P::two(da0 * u.x * ds0, da1 * u.y * ds1);
+            }
+            *reinterpret_cast<uint4*>(grow + j) = og;
+            *reinterpret_cast<uint4*>(urow + j) = ou;
+          }
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Shared-memory plan
+// ---------------------------------------------------------------------------
+template <int BN, int STAGES>
+struct TcSmem {
+  static constexpr int A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
+  static constexpr int B_BYTES = BN * TC_BK * 2;     // 32 KB for BN = 256
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+  // barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int MISC_OFFSET = BAR_OFFSET + NUM_BARS * 8;  // tmem slot, abort flag
+  static constexpr int TOTAL = MISC_OFFSET + 16;
+  static constexpr int DYN_BYTES = TOTAL + 1024;  // slack for 1024-byte alignment
+  static constexpr int TMEM_COLS = 2 * BN;        // power of two for BN in {128, 256}
+};
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <int BN, int STAGES, int A_MODE, int B_MODE, bool BF16, class Epi>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcShape s, const typename Epi::Params ep) {
+  using L = TcSmem<BN, STAGES>;
+  static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
+  static_assert(L::TOTAL + 1024 <= 232448, "shared memory plan exceeds 227 KB");
+
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment: the 128-byte swizzle pattern repeats every 1024 bytes
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::BAR_OFFSET;
+  auto full_bar = [&](int i) { return bar0 + 8u * i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (STAGES + i); };
+  auto accf_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + i); };
+  auto acce_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 + i); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFFSET);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFFSET + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(accf_bar(i), 1);
+      mbar_init(acce_bar(i), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = s.m_tiles * s.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;  // last load per stage
+      bool ok = true;
+      bool skip_once = s.inject_stall != 0;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int mt, nt;
+        tc_tile_coords(t, s, mt, nt);
+        const int m0 = mt * TC_BM;
+        for (int kb = 0; kb < s.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s.wait_limit_ns, abort_flag, s.err)) {
+            ok = false;
+            break;
+          }
+          if (skip_once) {
+            skip_once = false;  // fault injection: this stage never fills
+          } else {
+            const uint32_t sa = sbase + stage * L::STAGE_BYTES;
+            const uint32_t sb = sa + L::A_BYTES;
+            const int k0 = kb * TC_BK;
+            mbar_arrive_expect_tx(full_bar(stage), L::STAGE_BYTES);
+            if (A_MODE == LOAD_KMAJOR) {
+              tma_load_2d(sa, &tmA, full_bar(stage), k0, m0);
+            } else {
+#pragma unroll
+              for (int c = 0; c < TC_BM / 64; ++c)
+                tma_load_2d(sa + c * 8192, &tmA, full_bar(stage), m0 + 64 * c, k0);
+            }
+            if (B_MODE == LOAD_KMAJOR) {
+              tma_load_2d(sb, &tmB, full_bar(stage), k0, nt * BN);
+            } else if (B_MODE == LOAD_GATEUP) {
+              tma_load_3d(sb, &tmB, full_bar(stage), k0, nt * (BN / 2), 0);
+            } else {
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c)
+                tma_load_2d(sb + c * 8192, &tmB, full_bar(stage), nt * BN + 64 * c, k0);
+            }
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // unwinding: let the copies already issued land before the CTA exits
+        for (int i = 0; i < STAGES; ++i)
+          if (issued_mask & (1u << i))
+            mbar_wait_bounded(full_bar(i), (issued_parity >> i) & 1u, s.wait_limit_ns, nullptr,
+                              s.err);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc =
+          make_idesc_f16(BF16, A_MODE == LOAD_MNMAJOR, B_MODE == LOAD_MNMAJOR, TC_BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, s.wait_limit_ns, abort_flag, s.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < s.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, s.wait_limit_ns, abort_flag, s.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sbase + stage * L::STAGE_BYTES;
+          const uint32_t sb = sa + L::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < TC_BK / TC_UMMA_K; ++kk) {
+            const uint64_t ad = (A_MODE == LOAD_MNMAJOR)
+                                    ? make_sw128_desc(sa + kk * 2048, 8192, 1024)
+                                    : make_sw128_desc(sa + kk * 32, 16, 1024);
+            const uint64_t bd = (B_MODE == LOAD_MNMAJOR)
+                                    ? make_sw128_desc(sb + kk * 2048, 8192, 1024)
+                                    : make_sw128_desc(sb + kk * 32, 16, 1024);
+            umma_f16_ss(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(stage));  // frees the stage once these MMAs finish
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(accf_bar(acc));  // accumulator complete
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // drain: every MMA this thread issued has completed before TMEM is freed
+      umma_commit(drain_bar);
+      mbar_wait_bounded(drain_bar, 0, s.wait_limit_ns, nullptr, s.err);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      // one lane waits and the warp follows it: tcgen05.ld is warp-aligned
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_wait_bounded(accf_bar(acc), acc_phase, s.wait_limit_ns, abort_flag, s.err) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      int mt, nt;
+      tc_tile_coords(t, s, mt, nt);
+      const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      Epi::template run<BN, BF16>(ep, s, tacc, mt * TC_BM, nt, row);
+      tc_fence_before();
+      mbar_arrive(acce_bar(acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+}  // namespace swiglu

@@ -1,0 +1,156 @@
+/*
+ * swiglu_mlp.h -- C ABI of the fused SwiGLU MLP library for GB300 (sm_103a).
+ *
+ * The operation ("[RFC] Full-pipeline SwiGLU MLP with forward/backward
+ * co-optimization", Liger-Kernel issue #1347, section "Summary"):
+ *
+ *     G = X Wg^T,   U = X Wu^T,   A = SiLU(G) * U,   Y = A Wd^T
+ *
+ * and its gradients for Y's cotangent dY ("Correctness": dI = dX, dWg, dWu,
+ * dWd).  SiLU(g) = g / (1 + e^-g).
+ *
+ * Layouts (all row-major, nn.Linear convention):
+ *   X   [M, D]       M = B * S tokens
+ *   Wgu [2H, D]      rows 0..H-1 are Wg, rows H..2H-1 are Wu (the two
+ *                    projections concatenated, as one contiguous matrix)
+ *   Wd  [D, H]
+ *   Y   [M, D]
+ *   saved [M, 3H]    one contiguous buffer holding, per token row, [G | U | A]
+ *                    ("store A, G and U in one contiguous buffer", Summary)
+ *   dWgu [2H, D]     [dWg; dWu] in the layout of Wgu
+ *   dWd [D, H],  dX [M, D],  dY [M, D]
+ *
+ * Element types (swiglu_dtype): bf16 or fp16 storage with fp32 accumulation
+ * on the tensor cores, or SWIGLU_F32_IEEE: fp32 storage computed with IEEE
+ * fp32 FMA on the CUDA cores -- never TF32 ("[RFC] Testing Methodology for
+ * FP32 Convergence Tests on Fused SwiGLU/dSwiGLU Kernels", Liger-Kernel issue
+ * #1383, section "Root Cause").
+ *
+ * Rounding: G and U are rounded once to the storage type from the fp32
+ * accumulators; A = SiLU(G) * U is computed in fp32 from the unrounded
+ * accumulators and rounded once ("Scope one-round FP32 SwiGLU to the exact
+ * Qwen3.5 contract", xorl PR #51, review section); every other output is
+ * rounded once from its fp32 accumulator, round-to-nearest-even.
+ *
+ * Pointers: every tensor pointer is a DEVICE pointer, owned by the caller,
+ * 16-byte aligned.  Sizes: M >= 0, D >= 1, H >= 1; for bf16/fp16 D and H must
+ * be multiples of 8 (row strides of D, H, 2H and 3H elements are then
+ * multiples of 16 bytes, as the tensor-memory-access engine requires); for
+ * fp32 D and H must be multiples of 4.  M = 0 returns SWIGLU_OK and launches
+ * nothing.  ``stream`` is a cudaStream_t (0 = legacy default stream).
+ *
+ * Workspace: ``ws`` is a device buffer of at least swiglu_mlp_workspace_bytes()
+ * bytes, owned by the caller; the library keeps a device error word in it and
+ * clears it at the start of every call.  The library itself allocates no
+ * memory.
+ *
+ * Calls are asynchronous on ``stream`` and do not synchronise (except
+ * swiglu_mlp_query_error).  Argument errors are detected on the host before
+ * any launch and returned as a status; a device-side wait that runs past its
+ * time limit (a stuck pipeline) is recorded in the workspace error word and
+ * reported by swiglu_mlp_query_error as SWIGLU_ERR_DEVICE_TIMEOUT.
+ *
+ * Results are deterministic: no floating-point atomics; repeated calls on the
+ * same inputs give the same bits.
+ */
+#ifndef SWIGLU_MLP_H
+#define SWIGLU_MLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SWIGLU_BF16 = 0,
+  SWIGLU_F16 = 1,
+  SWIGLU_F32_IEEE = 2
+} swiglu_dtype;
+
+typedef enum {
+  SWIGLU_OK = 0,
+  SWIGLU_ERR_INVALID_ARG = 1,     /* null pointer, negative or zero size, bad enum */
+  SWIGLU_ERR_ALIGNMENT = 2,       /* pointer not 16-byte aligned, or D/H not a multiple of 8 (4 for fp32) */
+  SWIGLU_ERR_UNSUPPORTED = 3,     /* shape outside the supported range (e.g. > 2^31 - 1 rows) */
+  SWIGLU_ERR_WORKSPACE = 4,       /* ws is NULL or smaller than swiglu_mlp_workspace_bytes() */
+  SWIGLU_ERR_CUDA = 5,            /* a CUDA runtime/driver call or a launch failed */
+  SWIGLU_ERR_DEVICE_TIMEOUT = 6   /* a device pipeline wait ran past its limit */
+} swiglu_status;
+
+/* Operations, for sizing queries. */
+enum { SWIGLU_OP_FWD = 0, SWIGLU_OP_FWD_NOGRAD = 1, SWIGLU_OP_BWD = 2 };
+
+/* Bytes per element of a storage type (2, 2 or 4); 0 for an invalid value. */
+size_t swiglu_mlp_element_bytes(swiglu_dtype dtype);
+
+/* Bytes of the saved buffer: M * 3H elements ([G | U | A] per row). */
+size_t swiglu_mlp_saved_bytes(int64_t M, int64_t H, swiglu_dtype dtype);
+
+/* Bytes of workspace an operation needs (at least the 256-byte header that
+ * holds the device error word). */
+size_t swiglu_mlp_workspace_bytes(int64_t M, int64_t D, int64_t H, swiglu_dtype dtype, int op);
+
+/* Training forward.  Writes Y [M,D] and saved [M,3H] = [G | U | A].
+ * Reads X [M,D], Wgu [2H,D], Wd [D,H].  ("Summary": the gate and up
+ * projections fused with SiLU and gating in one kernel; A, G, U stored in one
+ * contiguous buffer.)  Kernels: gate/up + SwiGLU, then the down projection. */
+swiglu_status swiglu_mlp_fwd(const void* X, const void* Wgu, const void* Wd, void* Y,
+                             void* saved, int64_t M, int64_t D, int64_t H,
+                             swiglu_dtype dtype, void* ws, size_t ws_bytes, void* stream);
+
+/* Inference forward that saves neither G nor U ("Summary": a dedicated
+ * no-grad path).  Writes A [M,H] (row stride H) and Y [M,D]. */
+swiglu_status swiglu_mlp_fwd_nograd(const void* X, const void* Wgu, const void* Wd, void* Y,
+                                    void* A, int64_t M, int64_t D, int64_t H,
+                                    swiglu_dtype dtype, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward.  Consumes ``saved`` as written by swiglu_mlp_fwd on the same
+ * X, Wgu, Wd: the expired G/U columns are overwritten in place with dG/dU
+ * ("Summary": overwrite expired G/U storage with dG/dU; "Known limitations":
+ * hence no retain_graph and no second backward on the same buffer -- a second
+ * call on the same ``saved`` gives undefined values).
+ *   dA = dY Wd is never stored: dU = dA * SiLU(G), dG = dA * U * SiLU'(G)
+ *   with SiLU'(g) = s (1 + g (1 - s)), s = 1 / (1 + e^-g), G, U the stored
+ *   values;
+ *   dWd = dY^T A;  [dWg; dWu] = [dG | dU]^T X in one GEMM ("aggregate the dWg
+ *   and dWu computations into one GEMM");  dX = [dG | dU] [Wg; Wu] with one
+ *   accumulator over K = 2H ("compute dI in one fused kernel with a single
+ *   accumulator").
+ * Gradients are written, not accumulated (beta = 0).  Writes dX [M,D],
+ * dWgu [2H,D], dWd [D,H]; rewrites columns [0, 2H) of ``saved``. */
+swiglu_status swiglu_mlp_bwd(const void* dY, const void* X, const void* Wgu, const void* Wd,
+                             void* saved, void* dX, void* dWgu, void* dWd, int64_t M, int64_t D,
+                             int64_t H, swiglu_dtype dtype, void* ws, size_t ws_bytes,
+                             void* stream);
+
+/* Synchronises ``stream`` and reads the device error word in ``ws``:
+ * SWIGLU_OK, SWIGLU_ERR_DEVICE_TIMEOUT, or SWIGLU_ERR_CUDA if the stream
+ * reported an error. */
+swiglu_status swiglu_mlp_query_error(const void* ws, void* stream);
+
+/* Static description of a status code. */
+const char* swiglu_status_string(swiglu_status status);
+
+/* Limit, in nanoseconds, on every device-side pipeline wait of later calls
+ * from this process (default 2e9 = 2 s; values below 1000 are raised to
+ * 1000).  Returns the previous limit. */
+uint64_t swiglu_mlp_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook for failure detection: when ``on`` is nonzero, the next
+ * tensor-core launch of this process makes its load producer skip the arrival
+ * of the first pipeline stage, so the consumer's wait runs out, the kernel
+ * records SWIGLU_ERR_DEVICE_TIMEOUT and returns cleanly.  The flag clears
+ * itself after one launch.  Outputs of that call are undefined. */
+void swiglu_mlp_inject_stall_once(int on);
+
+/* Number of kernels the last fwd / fwd_nograd / bwd call launched on the
+ * device (for launch accounting in benchmarks). */
+int swiglu_mlp_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWIGLU_MLP_H */
