@@ -77,6 +77,12 @@ def lib() -> ctypes.CDLL:
         L.swiglu_mlp_inject_stall_once.argtypes = [ci]
         L.swiglu_mlp_last_launch_count.restype = ci
         L.swiglu_mlp_last_launch_count.argtypes = []
+        L.swiglu_mlp_profile_enable.restype = None
+        L.swiglu_mlp_profile_enable.argtypes = [ci]
+        L.swiglu_mlp_profile_read.restype = ci
+        L.swiglu_mlp_profile_read.argtypes = [ci, vp, vp]
+        L.swiglu_mlp_kernel_name.restype = ctypes.c_char_p
+        L.swiglu_mlp_kernel_name.argtypes = [ci]
         _lib = L
         return L
 
@@ -196,3 +202,23 @@ def swiglu_mlp_inject_stall_once(on: bool = True) -> None:
 
 def swiglu_mlp_last_launch_count() -> int:
     return int(lib().swiglu_mlp_last_launch_count())
+
+
+def swiglu_mlp_profile_enable(on: bool = True) -> None:
+    lib().swiglu_mlp_profile_enable(1 if on else 0)
+
+
+def swiglu_mlp_profile_read() -> dict:
+    """{kernel name: (launches, total device ms)} since the previous read."""
+    n = 64
+    launches = (ctypes.c_int64 * n)()
+    ms = (ctypes.c_double * n)()
+    k = lib().swiglu_mlp_profile_read(n, ctypes.cast(launches, ctypes.c_void_p),
+                                      ctypes.cast(ms, ctypes.c_void_p))
+    if k < 0:
+        raise SwigluError(5, "swiglu_mlp_profile_read")
+    out = {}
+    for i in range(k):
+        if launches[i]:
+            out[lib().swiglu_mlp_kernel_name(i).decode()] = (int(launches[i]), float(ms[i]))
+    return out

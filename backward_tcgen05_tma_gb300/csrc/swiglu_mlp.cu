@@ -17,6 +17,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/swiglu_mlp.h"
 #include "simt_gemm.cuh"
@@ -33,6 +34,58 @@ constexpr int TC_BN = 256;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_last_launches{0};
+
+// ---------------------------------------------------------------------------
+// optional per-kernel timing: CUDA events bracket each launch on its stream
+// ---------------------------------------------------------------------------
+enum KernelId : int {
+  K_GATE_UP = 0, K_DOWN, K_DGU, K_DWD, K_DWGU, K_DX, K_GATE_UP_NOGRAD, K_DOWN_NOGRAD,
+  K_SIMT_GATE_UP, K_SIMT_DOWN, K_SIMT_DGU, K_SIMT_DWD, K_SIMT_DWGU, K_SIMT_DX, K_COUNT
+};
+const char* const kKernelNames[K_COUNT] = {
+    "gate_up_swiglu", "down_proj", "dgu_inplace", "dwd", "dwgu", "dx", "gate_up_nograd",
+    "down_proj_nograd", "simt_gate_up_swiglu", "simt_down_proj", "simt_dgu_inplace", "simt_dwd",
+    "simt_dwgu", "simt_dx"};
+
+struct ProfRec {
+  int id;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+std::atomic<int> g_prof_on{0};
+std::vector<ProfRec> g_prof_pending;
+std::vector<cudaEvent_t> g_prof_pool;
+double g_prof_ms[K_COUNT];
+int64_t g_prof_n[K_COUNT];
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Brackets one launch with events when timing is enabled.
+struct ProfScope {
+  int id;
+  cudaStream_t st;
+  cudaEvent_t b = nullptr;
+  ProfScope(int id_, cudaStream_t st_) : id(id_), st(st_) {
+    if (!g_prof_on.load()) return;
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    cudaEvent_t a = prof_event();
+    b = prof_event();
+    cudaEventRecord(a, st);
+    g_prof_pending.push_back(ProfRec{id, a, b});
+  }
+  ~ProfScope() {
+    if (b != nullptr) cudaEventRecord(b, st);
+  }
+};
 
 // ---------------------------------------------------------------------------
 // driver entry point for tensor-map encoding (no link-time libcuda dependency)
@@ -121,7 +174,7 @@ TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err
 }
 
 template <int AM, int BMODE, bool BF16, class Epi>
-cudaError_t launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const TcShape& s,
+cudaError_t launch_tc(int kid, const CUtensorMap& ta, const CUtensorMap& tb, const TcShape& s,
                       const typename Epi::Params& ep, cudaStream_t st) {
   auto kern = tc_gemm_kernel<TC_BN, TC_STAGES, AM, BMODE, BF16, Epi>;
   constexpr int smem = TcSmem<TC_BN, TC_STAGES>::DYN_BYTES;
@@ -130,15 +183,17 @@ cudaError_t launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const TcShap
   const int tiles = s.m_tiles * s.n_tiles;
   const int nsm = sm_count();
   const int grid = tiles < nsm ? tiles : nsm;
+  ProfScope prof(kid, st);
   kern<<<grid, TC_THREADS, smem, st>>>(ta, tb, s, ep);
   g_last_launches.fetch_add(1);
   return cudaGetLastError();
 }
 
 template <bool DUAL, class Epi>
-cudaError_t launch_simt(SimtOperand A, SimtOperand B, SimtOperand B2, int64_t M, int64_t N,
-                        int64_t K, const Epi& epi, cudaStream_t st) {
+cudaError_t launch_simt(int kid, SimtOperand A, SimtOperand B, SimtOperand B2, int64_t M,
+                        int64_t N, int64_t K, const Epi& epi, cudaStream_t st) {
   dim3 grid((unsigned)((N + SG_BN - 1) / SG_BN), (unsigned)((M + SG_BM - 1) / SG_BM));
+  ProfScope prof(kid, st);
   simt_gemm_kernel<DUAL, Epi><<<grid, SG_THREADS, 0, st>>>(A, B, B2, (int)M, (int)N, (int)K, epi);
   g_last_launches.fetch_add(1);
   return cudaGetLastError();
@@ -194,14 +249,16 @@ swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y
     return SWIGLU_ERR_CUDA;
   TcShape s1 = make_shape(M, H, D, TC_BN / 2, err);
   EpiSwiGLU::Params p1{G, U, ld_gu, A, ld_a};
-  cudaError_t e = launch_tc<LOAD_KMAJOR, LOAD_GATEUP, BF16, EpiSwiGLU>(tx, tw, s1, p1, st);
+  cudaError_t e = launch_tc<LOAD_KMAJOR, LOAD_GATEUP, BF16, EpiSwiGLU>(
+      G != nullptr ? K_GATE_UP : K_GATE_UP_NOGRAD, tx, tw, s1, p1, st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   // down projection: Y = A Wd^T
   if (!map_kmajor(&ta, BF16, A, H, M, ld_a, TC_BM) || !map_kmajor(&twd, BF16, Wd, H, D, H, TC_BN))
     return SWIGLU_ERR_CUDA;
   TcShape s2 = make_shape(M, D, H, TC_BN, err);
   EpiStore::Params p2{Y, D};
-  return cuda_status(launch_tc<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore>(ta, twd, s2, p2, st));
+  return cuda_status(launch_tc<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore>(
+      G != nullptr ? K_DOWN : K_DOWN_NOGRAD, ta, twd, s2, p2, st));
 }
 
 template <bool BF16>
@@ -221,7 +278,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   {
     TcShape s = make_shape(M, H, D, TC_BN, err);
     EpiDSwiGLU::Params p{G, U, ld};
-    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLU>(m1, m2, s, p, st);
+    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLU>(K_DGU, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   // dWd [D, H] = dY^T A: both operands MN-major over the token dimension
@@ -230,7 +287,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   {
     TcShape s = make_shape(D, H, M, TC_BN, err);
     EpiStore::Params p{dWd, H};
-    e = launch_tc<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(m1, m2, s, p, st);
+    e = launch_tc<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DWD, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   // [dWg; dWu] [2H, D] = [dG | dU]^T X: one GEMM over the 2H columns
@@ -239,7 +296,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   {
     TcShape s = make_shape(2 * H, D, M, TC_BN, err);
     EpiStore::Params p{dWgu, D};
-    e = launch_tc<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(m1, m2, s, p, st);
+    e = launch_tc<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DWGU, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   // dX [M, D] = [dG | dU] [Wg; Wu]: K = 2H in one accumulator
@@ -248,7 +305,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   {
     TcShape s = make_shape(M, D, 2 * H, TC_BN, err);
     EpiStore::Params p{dX, D};
-    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(m1, m2, s, p, st);
+    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DX, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   return SWIGLU_OK;
@@ -261,10 +318,10 @@ swiglu_status simt_forward(const float* X, const float* Wgu, const float* Wd, fl
                            float* U, int64_t ld_gu, float* A, int64_t ld_a, int64_t M, int64_t D,
                            int64_t H, cudaStream_t st) {
   SimtOperand x{X, D, 1}, wg{Wgu, D, 1}, wu{Wgu + H * D, D, 1};
-  cudaError_t e = launch_simt<true>(x, wg, wu, M, H, D, SimtEpiSwiGLU{G, U, ld_gu, A, ld_a}, st);
+  cudaError_t e = launch_simt<true>(K_SIMT_GATE_UP, x, wg, wu, M, H, D, SimtEpiSwiGLU{G, U, ld_gu, A, ld_a}, st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   SimtOperand a{A, ld_a, 1}, wd{Wd, H, 1};
-  return cuda_status(launch_simt<false>(a, wd, wd, M, D, H, SimtEpiStore{Y, D}, st));
+  return cuda_status(launch_simt<false>(K_SIMT_DOWN, a, wd, wd, M, D, H, SimtEpiStore{Y, D}, st));
 }
 
 swiglu_status simt_backward(const float* dY, const float* X, const float* Wgu, const float* Wd,
@@ -276,19 +333,19 @@ swiglu_status simt_backward(const float* dY, const float* X, const float* Wgu, c
   float* A = saved + 2 * H;
   cudaError_t e;
   // dA = dY Wd: A(m, d) = dY[m, d]; B(j, d) = Wd[d, j]
-  e = launch_simt<false>(SimtOperand{dY, D, 1}, SimtOperand{Wd, 1, H}, SimtOperand{Wd, 1, H}, M,
+  e = launch_simt<false>(K_SIMT_DGU, SimtOperand{dY, D, 1}, SimtOperand{Wd, 1, H}, SimtOperand{Wd, 1, H}, M,
                          H, D, SimtEpiDSwiGLU{G, U, ld}, st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   // dWd[d, j] = sum_m dY[m, d] A[m, j]
-  e = launch_simt<false>(SimtOperand{dY, 1, D}, SimtOperand{A, 1, ld}, SimtOperand{A, 1, ld}, D,
+  e = launch_simt<false>(K_SIMT_DWD, SimtOperand{dY, 1, D}, SimtOperand{A, 1, ld}, SimtOperand{A, 1, ld}, D,
                          H, M, SimtEpiStore{dWd, H}, st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   // dWgu[j', d] = sum_m dGU[m, j'] X[m, d]
-  e = launch_simt<false>(SimtOperand{G, 1, ld}, SimtOperand{X, 1, D}, SimtOperand{X, 1, D}, 2 * H,
+  e = launch_simt<false>(K_SIMT_DWGU, SimtOperand{G, 1, ld}, SimtOperand{X, 1, D}, SimtOperand{X, 1, D}, 2 * H,
                          D, M, SimtEpiStore{dWgu, D}, st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   // dX[m, d] = sum_j' dGU[m, j'] Wgu[j', d]
-  e = launch_simt<false>(SimtOperand{G, ld, 1}, SimtOperand{Wgu, 1, D}, SimtOperand{Wgu, 1, D}, M,
+  e = launch_simt<false>(K_SIMT_DX, SimtOperand{G, ld, 1}, SimtOperand{Wgu, 1, D}, SimtOperand{Wgu, 1, D}, M,
                          D, 2 * H, SimtEpiStore{dX, D}, st);
   return cuda_status(e);
 }
@@ -421,5 +478,33 @@ uint64_t swiglu_mlp_set_wait_limit_ns(uint64_t ns) {
 void swiglu_mlp_inject_stall_once(int on) { g_inject_stall.store(on ? 1 : 0); }
 
 int swiglu_mlp_last_launch_count(void) { return g_last_launches.load(); }
+
+void swiglu_mlp_profile_enable(int on) { g_prof_on.store(on ? 1 : 0); }
+
+int swiglu_mlp_profile_read(int n, int64_t* launches, double* total_ms) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  int rc = K_COUNT;
+  for (const ProfRec& r : g_prof_pending) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
+      rc = -1;
+    g_prof_ms[r.id] += ms;
+    g_prof_n[r.id] += 1;
+    g_prof_pool.push_back(r.a);
+    g_prof_pool.push_back(r.b);
+  }
+  g_prof_pending.clear();
+  for (int i = 0; i < K_COUNT && i < n; ++i) {
+    if (launches) launches[i] = g_prof_n[i];
+    if (total_ms) total_ms[i] = g_prof_ms[i];
+    g_prof_n[i] = 0;
+    g_prof_ms[i] = 0.0;
+  }
+  return rc;
+}
+
+const char* swiglu_mlp_kernel_name(int id) {
+  return (id >= 0 && id < K_COUNT) ? kKernelNames[id] : nullptr;
+}
 
 }  // extern "C"

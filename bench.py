@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Benchmark of the fused SwiGLU MLP forward + backward on GB300.
+
+Metric: fwd+bwd TFLOPS with the pages' FLOP convention 18 M D H (M = B S) and
+its fraction of the measured dense-bf16 tensor peak.  Workload: B=8, S=8192,
+D=4096, H=11008, bf16 storage with fp32 accumulation, seeded synthetic data
+(X ~ N(0,1), Wg/Wu ~ N(0,1/D), Wd ~ N(0,1/H), dY ~ N(0,1e-2)).
+
+One step = swiglu_mlp_fwd + swiglu_mlp_bwd (all six kernels) on device-resident
+inputs; every input is larger than the 129 MB L2, so no flush is needed.
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs an independent
+replica (the path has no exchange step on one GPU): value = all ranks' FLOPs /
+the slowest rank's time.
+
+--impl reference times the CPU fp64 oracle on a bounded token sample of the
+same workload (the reference arm); only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    "B8_S8192_D4096_H11008": dict(B=8, S=8192, D=4096, H=11008),
+    "B8_S4096_D2048_H5632": dict(B=8, S=4096, D=2048, H=5632),
+    "B8_S2048_D1024_H2816": dict(B=8, S=2048, D=1024, H=2816),
+}
+MAIN = "B8_S8192_D4096_H11008"
+# the pages' own number for this workload: 1049.66 ms on an RTX 5060 Ti
+# (SM120), i.e. 18 M D H / t = 50.67 TFLOPS ("Training results" table)
+PAGES_TFLOPS = {MAIN: 18.0 * 65536 * 4096 * 11008 / 1.04966 / 1e12}
+NOGRAD_S = [1, 2, 4, 8, 16, 32, 64, 128, 256]
+CPU_SAMPLE_TOKENS = 16
+REF_STEP_TOKENS = 8
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def _csrc_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "backward_tcgen05_tma_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel: str, workload: str):
+    """dram read+write bytes per launch from the committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    e = t.get(workload, {}).get(kernel)
+    if not e or e.get("csrc_hash") != _csrc_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _config(workload, w, dtype, world):
+    return {"workload": workload, "B": w["B"], "S": w["S"], "D": w["D"], "H": w["H"],
+            "M": w["B"] * w["S"], "dtype": dtype, "parallelism": "replicas%d" % world,
+            "l2": "inputs larger than L2 (no flush)"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import torch
+
+    import oracle
+    from backward_tcgen05_tma_gb300 import metrics, synthetic
+    w = WORKLOADS[args.workload]
+    D, H = w["D"], w["H"]
+    m = REF_STEP_TOKENS
+    t = synthetic.make_inputs(m, D, H, "bf16", seed=0, device="cpu", kind="device")
+    cores = oracle.num_threads()
+
+    def step():
+        f = oracle.forward(t["X"], t["Wg"], t["Wu"], t["Wd"])
+        oracle.backward(t["dY"], t["X"], t["Wg"], t["Wu"], t["Wd"], f)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = metrics.fwd_bwd_flops(m, D, H) / dt / 1e12
+    sample = ("fwd+bwd of %d token rows per step through the fp64 oracle, full D=%d, H=%d "
+              "weights of the workload" % (m, D, H))
+    line = {"impl": "reference", "metric": "SwiGLU MLP fwd+bwd TFLOPS (18*M*D*H)",
+            "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(args.workload, w, "bf16", world),
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def _alloc(M, D, H, dt, device):
+    import torch
+    from backward_tcgen05_tma_gb300 import api
+    e = {"Y": torch.empty(M, D, dtype=dt, device=device),
+         "saved": torch.empty(M, 3 * H, dtype=dt, device=device),
+         "dX": torch.empty(M, D, dtype=dt, device=device),
+         "dWgu": torch.empty(2 * H, D, dtype=dt, device=device),
+         "dWd": torch.empty(D, H, dtype=dt, device=device)}
+    e["ws"] = api.workspace(M, D, H, dt, api.SWIGLU_OP_BWD, device)
+    return e
+
+
+def _step(api, t, o):
+    api.swiglu_mlp_fwd(t["X"], t["Wgu"], t["Wd"], out=o, ws=o["ws"])
+    n = api.swiglu_mlp_last_launch_count()
+    api.swiglu_mlp_bwd(t["dY"], t["X"], t["Wgu"], t["Wd"], o["saved"], out=o, ws=o["ws"])
+    return n + api.swiglu_mlp_last_launch_count()
+
+
+def _kernel_flops(name, M, D, H):
+    return {"gate_up_swiglu": 2.0 * M * 2 * H * D, "down_proj": 2.0 * M * D * H,
+            "dgu_inplace": 2.0 * M * H * D, "dwd": 2.0 * D * H * M,
+            "dwgu": 2.0 * 2 * H * D * M, "dx": 2.0 * M * D * 2 * H}[name]
+
+
+def _time_training(api, w, dtype_name, steps, warmup, seed, device, profile=False):
+    """Times `steps` fwd+bwd steps; returns (seconds per step, launches, profile)."""
+    import torch
+    from backward_tcgen05_tma_gb300 import synthetic
+    dt = {"bf16": torch.bfloat16, "f16": torch.float16}[dtype_name]
+    M, D, H = w["B"] * w["S"], w["D"], w["H"]
+    t = synthetic.make_inputs(M, D, H, dtype_name, seed=seed, device=device, kind="device")
+    o = _alloc(M, D, H, dt, device)
+    for _ in range(warmup):
+        _step(api, t, o)
+    torch.cuda.synchronize()
+    if profile:
+        api.swiglu_mlp_profile_read()
+        api.swiglu_mlp_profile_enable(True)
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    e0.record(st)
+    for _ in range(steps):
+        launches += _step(api, t, o)
+    e1.record(st)
+    torch.cuda.synchronize()
+    prof = None
+    if profile:
+        api.swiglu_mlp_profile_enable(False)
+        prof = api.swiglu_mlp_profile_read()
+    return e0.elapsed_time(e1) / 1e3 / steps, launches, prof, (t, o)
+
+
+def _e2e(api, t, o, steps):
+    """Same step with host inputs/outputs: pinned H2D of X, dY and D2H of
+    Y, dX, dWgu, dWd inside the timed region."""
+    import torch
+    hx = torch.empty_like(t["X"], device="cpu").pin_memory()
+    hdy = torch.empty_like(t["dY"], device="cpu").pin_memory()
+    hx.copy_(t["X"])
+    hdy.copy_(t["dY"])
+    outs = {k: torch.empty_like(o[k], device="cpu").pin_memory() for k in ("Y", "dX", "dWgu", "dWd")}
+    h2d = hx.numel() * hx.element_size() + hdy.numel() * hdy.element_size()
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+
+    def one():
+        t["X"].copy_(hx, non_blocking=True)
+        t["dY"].copy_(hdy, non_blocking=True)
+        _step(api, t, o)
+        for k, v in outs.items():
+            v.copy_(o[k], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        one()
+    e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / steps, h2d, d2h
+
+
+def _nograd_sweep(api, device, peaks):
+    import torch
+    from backward_tcgen05_tma_gb300 import metrics, synthetic
+    D, H = 4096, 11008
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)  # 512 MiB > L2
+    wts = synthetic.make_inputs(1, D, H, "bf16", seed=1, device=device, kind="device")
+    res = []
+    for S in NOGRAD_S:
+        X = synthetic.device_normal((S, D), 1.0, "bf16", 1, 0, device)
+        Y = torch.empty(S, D, dtype=torch.bfloat16, device=device)
+        A = torch.empty(S, H, dtype=torch.bfloat16, device=device)
+        ws = api.workspace(S, D, H, torch.bfloat16, api.SWIGLU_OP_FWD_NOGRAD, device)
+        o = {"Y": Y, "A": A}
+        for _ in range(3):
+            api.swiglu_mlp_fwd_nograd(X, wts["Wgu"], wts["Wd"], out=o, ws=ws)
+        times = []
+        st = torch.cuda.current_stream()
+        for _ in range(20):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            api.swiglu_mlp_fwd_nograd(X, wts["Wgu"], wts["Wd"], out=o, ws=ws)
+            e1.record(st)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) / 1e3)
+        tmed = statistics.median(times)
+        byts = metrics.nograd_algorithmic_bytes(S, D, H)
+        res.append({"S": S, "us": round(tmed * 1e6, 2), "GBps": round(byts / tmed / 1e9, 1),
+                    "hbm_frac": round(byts / tmed / 1e9 / peaks["hbm_gbs"], 4),
+                    "TFLOPS": round(metrics.fwd_flops(S, D, H) / tmed / 1e12, 2)})
+    return {"workload": "B1_D4096_H11008_bf16_nograd", "l2": "flushed (512 MiB write) before "
+            "each timed call", "median_of": 20, "sweep": res}
+
+
+def _cpu_baseline(t_dev, w):
+    """The oracle, as it stands, on a bounded sample: fwd+bwd of the first
+    CPU_SAMPLE_TOKENS token rows of the workload with its full weights."""
+    import oracle
+    from backward_tcgen05_tma_gb300 import metrics
+    m = CPU_SAMPLE_TOKENS
+    D, H = w["D"], w["H"]
+    c = {k: t_dev[k][:m].cpu() if k in ("X", "dY") else t_dev[k].cpu()
+         for k in ("X", "dY", "Wg", "Wu", "Wd")}
+    t0 = time.perf_counter()
+    f = oracle.forward(c["X"], c["Wg"], c["Wu"], c["Wd"])
+    oracle.backward(c["dY"], c["X"], c["Wg"], c["Wu"], c["Wd"], f)
+    dt = time.perf_counter() - t0
+    return {"value": metrics.fwd_bwd_flops(m, D, H) / dt / 1e12, "unit": "TFLOPS",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "fwd+bwd of %d token rows (full D=%d, H=%d weights) of the workload, "
+                      "fp64 loops, %.1f s" % (m, D, H, dt)}
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    device = "cuda:%d" % local
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(device))
+    from backward_tcgen05_tma_gb300 import api, build, metrics
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    api.lib()
+    peaks = _peaks()
+    w = WORKLOADS[args.workload]
+    M, D, H = w["B"] * w["S"], w["D"], w["H"]
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sec, launches, prof, (t, o) = _time_training(api, w, "bf16", args.steps, args.warmup,
+                                                 seed=rank, device=device, profile=True)
+    clocks = sampler.stop()
+    if world > 1:
+        mx = torch.tensor([sec], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
+        sec = float(mx.item())
+        torch.distributed.barrier()
+    flops = metrics.fwd_bwd_flops(M, D, H)
+    value = flops * world / sec / 1e12
+
+    # dominant kernel from live event timings of the timed region
+    dom = max(prof.items(), key=lambda kv: kv[1][1])
+    name, (n_l, ms) = dom
+    per_launch_s = ms / 1e3 / n_l
+    achieved = _kernel_flops(name, M, D, H) / per_launch_s / 1e12
+    traffic = _traffic(name, args.workload)
+    kernels = {k: {"launches": v[0], "ms_per_launch": round(v[1] / v[0], 4),
+                   "share": round(v[1] / sum(x[1] for x in prof.values()), 4),
+                   "TFLOPS": round(_kernel_flops(k, M, D, H) / (v[1] / 1e3 / v[0]) / 1e12, 1)}
+               for k, v in prof.items()}
+
+    e2e_sec, h2d, d2h = _e2e(api, t, o, max(2, args.steps // 2))
+    del t, o
+    torch.cuda.empty_cache()
+
+    line = {"metric": "SwiGLU MLP fwd+bwd TFLOPS (18*M*D*H)", "value": value, "unit": "TFLOPS",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": value / world / PAGES_TFLOPS[args.workload]
+            if args.workload in PAGES_TFLOPS else None,
+            "dtype": "bf16", "data": "synthetic (seeded, device generator)",
+            "config": _config(args.workload, w, "bf16", world),
+            "pct_of_bf16_peak": {"burst": value / world / peaks["bf16_tflops"],
+                                 "sustained": value / world / peaks["bf16_tflops_sustained"],
+                                 "source": peaks["source"]},
+            "roofline": {"bound": "tensor", "kernel": name, "achieved": achieved,
+                         "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16_tflops_sustained"],
+                         "peak_kind": "bf16 sustained (%s)" % peaks["source"],
+                         "traffic": traffic},
+            "kernels": kernels,
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "e2e": {"value": flops / e2e_sec / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_sec * 1e3}}
+
+    if world == 1 and not args.quick:
+        extra = {}
+        for wl, dts in (("B8_S2048_D1024_H2816", ["bf16"]), ("B8_S4096_D2048_H5632", ["bf16", "f16"])):
+            for dn in dts:
+                s2, _, _, keep = _time_training(api, WORKLOADS[wl], dn, 10, 3, 0, device)
+                del keep
+                w2 = WORKLOADS[wl]
+                f2 = metrics.fwd_bwd_flops(w2["B"] * w2["S"], w2["D"], w2["H"])
+                extra["%s_%s" % (wl, dn)] = {"ms_per_step": round(s2 * 1e3, 3),
+                                             "TFLOPS": round(f2 / s2 / 1e12, 1)}
+                torch.cuda.empty_cache()
+        line["other_workloads"] = extra
+        line["nograd"] = _nograd_sweep(api, device, peaks)
+    if world == 1 or rank == 0:
+        if world == 1 and not args.no_cpu:
+            from backward_tcgen05_tma_gb300 import synthetic
+            tc = synthetic.make_inputs(CPU_SAMPLE_TOKENS, D, H, "bf16", seed=0, device=device,
+                                       kind="device")
+            line["cpu_baseline"] = _cpu_baseline(tc, w)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=MAIN)
+    ap.add_argument("--quick", action="store_true", help="main workload only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

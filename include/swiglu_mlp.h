@@ -149,6 +149,19 @@ void swiglu_mlp_inject_stall_once(int on);
  * device (for launch accounting in benchmarks). */
 int swiglu_mlp_last_launch_count(void);
 
+/* Per-kernel device timing for benchmarks.  While enabled, every kernel
+ * launch is bracketed by two CUDA events recorded on its stream (do not
+ * enable it during CUDA-graph stream capture).  swiglu_mlp_profile_read waits
+ * for the recorded events, writes, for kernel ids 0 .. n-1, the number of
+ * launches and their summed device time in milliseconds since the previous
+ * read (either array may be NULL), resets the counters, and returns the
+ * number of kernel ids (-1 if an event could not be read). */
+void swiglu_mlp_profile_enable(int on);
+int swiglu_mlp_profile_read(int n, int64_t* launches, double* total_ms);
+
+/* Name of a kernel id (NULL outside 0 .. count-1). */
+const char* swiglu_mlp_kernel_name(int id);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,85 @@
+"""Host-side checks of the C-ABI library: it builds for sm_103a, loads, exports
+every declared entry point, and rejects bad arguments before any CUDA call.
+No GPU needed (no compute call is made)."""
+import ctypes
+
+import pytest
+
+from backward_tcgen05_tma_gb300 import api, build
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+OK, INVALID, ALIGN, UNSUP, WSERR = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return api.lib()
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = api.declared_symbols()
+    for must in ("swiglu_mlp_fwd", "swiglu_mlp_fwd_nograd", "swiglu_mlp_bwd",
+                 "swiglu_mlp_query_error", "swiglu_status_string", "swiglu_mlp_workspace_bytes",
+                 "swiglu_mlp_saved_bytes"):
+        assert must in names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_sizes(L):
+    assert L.swiglu_mlp_element_bytes(0) == 2
+    assert L.swiglu_mlp_element_bytes(1) == 2
+    assert L.swiglu_mlp_element_bytes(2) == 4
+    assert L.swiglu_mlp_element_bytes(7) == 0
+    # saved = [G | U | A] = M * 3H elements
+    assert L.swiglu_mlp_saved_bytes(65536, 11008, 0) == 65536 * 3 * 11008 * 2
+    assert L.swiglu_mlp_saved_bytes(32, 176, 2) == 32 * 528 * 4
+    for op in (0, 1, 2):
+        assert L.swiglu_mlp_workspace_bytes(65536, 4096, 11008, 0, op) >= 4
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert api.status_string(code)
+    assert "timed out" in api.status_string(6)
+
+
+P = ctypes.c_void_p(0x10000)          # an aligned fake device address (never dereferenced)
+P_MIS = ctypes.c_void_p(0x10002)
+N = ctypes.c_void_p(0)
+
+
+def _fwd(L, X=P, W=P, Wd=P, Y=P, S=P, M=128, D=64, H=128, dt=0, ws=P, wsb=256):
+    return L.swiglu_mlp_fwd(X, W, Wd, Y, S, M, D, H, dt, ws, wsb, N)
+
+
+def test_argument_errors_are_reported_before_any_launch(L):
+    assert _fwd(L, X=N) == INVALID
+    assert _fwd(L, Y=N) == INVALID
+    assert _fwd(L, D=0) == INVALID
+    assert _fwd(L, H=-8) == INVALID
+    assert _fwd(L, M=-1) == INVALID
+    assert _fwd(L, dt=9) == INVALID
+    assert _fwd(L, X=P_MIS) == ALIGN
+    assert _fwd(L, D=60) == ALIGN          # bf16 needs D % 8 == 0
+    assert _fwd(L, H=124) == ALIGN
+    assert _fwd(L, ws=N) == WSERR
+    assert _fwd(L, wsb=8) == WSERR
+    assert _fwd(L, M=2 ** 31) == UNSUP
+    assert L.swiglu_mlp_fwd_nograd(N, P, P, P, P, 4, 64, 128, 0, P, 256, N) == INVALID
+    assert L.swiglu_mlp_bwd(P, P, P, P, P, P, P, N, 4, 64, 128, 0, P, 256, N) == INVALID
+    assert L.swiglu_mlp_bwd(P, P, P, P, P, P, P, P_MIS, 4, 64, 128, 0, P, 256, N) == ALIGN
+
+
+def test_empty_batch_is_ok_without_launch(L):
+    assert _fwd(L, M=0) == OK
+    assert L.swiglu_mlp_fwd_nograd(P, P, P, P, P, 0, 64, 128, 0, P, 256, N) == OK
+    assert L.swiglu_mlp_bwd(P, P, P, P, P, P, P, P, 0, 64, 128, 1, P, 256, N) == OK
+    assert L.swiglu_mlp_last_launch_count() == 0
+
+
+def test_wait_limit_setter(L):
+    old = api.swiglu_mlp_set_wait_limit_ns(5)
+    assert api.swiglu_mlp_set_wait_limit_ns(old) == 1000  # clamped to 1 us
