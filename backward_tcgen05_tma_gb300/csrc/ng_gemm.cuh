@@ -1,0 +1,440 @@
+// ng_gemm.cuh -- the no-grad forward for a handful of tokens (M <= 64), where
+// the work is bound by streaming the weights from HBM, not by the tensor core.
+//
+// Swap-AB: 128 weight rows take the MMA's M dimension and the (padded) tokens
+// its N dimension (NT = 16, 32 or 64), so one tcgen05.mma M=128 x N=NT x K=16
+// consumes 4 KB of weights.  The weight stream is spread evenly over every
+// SM by a stream-K decomposition: the tiles' k-blocks are laid end to end
+// (tile-major) and each persistent CTA (one per SM) takes one contiguous
+// range of that sequence, so every CTA streams the same number of bytes and
+// its TMA ring never drains between tiles.  A range cuts a tile into
+// segments; each segment's fp32 partial tile goes to the workspace (slot =
+// CTA x segment index), two TMEM accumulators let the epilogue of one segment
+// overlap the MMAs of the next, and the last CTA of a tile to finish (per-tile
+// arrival counter) sums the tile's partials in CTA order -- deterministic --
+// and applies the epilogue:
+//   gate/up: tile = 64 hidden units; rows 0..63 are Wg rows, 64..127 the Wu
+//            rows of the same units (one 3-D TMA box), so the partial sums of
+//            G and U meet in one CTA: A = rnd(SiLU(g) * u) -> A [M, H];
+//   down:    tile = 128 output features of Wd; Y = rnd(sum) -> Y [M, D].
+// No CTA ever waits for another CTA: a segment that is not last moves on.
+// The down kernel is launched as a programmatic dependent of the gate/up
+// kernel: its CTAs start streaming Wd into the ring while gate/up drains, and
+// wait (griddepcontrol.wait) only before touching anything gate/up writes.
+#pragma once
+
+#include "tc_gemm.cuh"
+
+namespace swiglu {
+
+struct NgArgs {
+  int M;            // tokens (<= NT)
+  int rows;         // gate/up: H (hidden units); down: D (output features)
+  int kb_tile;      // k-blocks of 64 in one tile's contraction
+  int tiles;
+  int seg_max;      // partial slots per CTA (>= segments of any CTA's range)
+  float* part;      // [gridDim.x * seg_max][128][NT] fp32 partial tiles
+  int* counters;    // [tiles] arrival counters, zero at launch
+  int* zero_ptr;    // block 0 zeroes zero_ptr[0 .. zero_count): the other
+  int zero_count;   //   kernel's counters (after the dependency wait)
+  int clear_err;    // block 0 clears the error word at start (first kernel of a call)
+  int dependent;    // launched as a programmatic dependent of the gate/up kernel
+  void* out;        // A [M, ld_out] or Y [M, ld_out]
+  int64_t ld_out;
+  uint64_t wait_limit_ns;
+  int* err;
+};
+
+template <int NT>
+struct NgSmem {
+  static constexpr int W_BYTES = 128 * 64 * 2;  // 16 KB of weights per k-block
+  static constexpr int X_BYTES = NT * 64 * 2;   // the tokens' k-block
+  static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;  // ~200 KB of weights in flight
+  static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, acc_full[2], acc_empty[2], drain
+  static constexpr int MISC_OFFSET = BAR_OFFSET + NUM_BARS * 8;
+  static constexpr int TOTAL = MISC_OFFSET + 16;
+  static constexpr int DYN_BYTES = TOTAL + 1024;
+  static constexpr int TMEM_COLS = 2 * NT < 32 ? 32 : 2 * NT;
+};
+
+// Named barrier 1 over the 128 epilogue threads (warps 2..5).
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Stream-K partition: CTA c owns global k-blocks [ng_start(c), ng_start(c+1)).
+__device__ __forceinline__ int64_t ng_start(int64_t c, int64_t total, int64_t ctas) {
+  return c * total / ctas;
+}
+
+// The CTA whose range holds global k-block x.
+__device__ __forceinline__ int ng_owner(int64_t x, int64_t total, int64_t ctas) {
+  int64_t c = x * ctas / total;
+  while (c + 1 < ctas && ng_start(c + 1, total, ctas) <= x) ++c;
+  while (c > 0 && ng_start(c, total, ctas) > x) --c;
+  return (int)c;
+}
+
+// Same barrier, returning the AND of v over the 128 threads, so that every
+// epilogue warp takes the same branch afterwards.
+__device__ __forceinline__ int epi_bar_and(int v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(v)
+      : "memory");
+  return r;
+}
+
+template <int NT, bool GATE_UP, bool BF16>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    ng_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const NgArgs a) {
+  using L = NgSmem<NT>;
+  static_assert(NT == 16 || NT == 32 || NT == 64, "NT must be 16, 32 or 64");
+  static_assert(L::TOTAL + 1024 <= 232448, "shared memory plan exceeds 227 KB");
+  constexpr int TILE_ROWS = GATE_UP ? 64 : 128;  // output rows (hidden units / features) per tile
+  constexpr int RB = NT <= 16 ? 4 : (NT <= 32 ? 2 : 1);  // partials loaded per reduction batch
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::BAR_OFFSET;
+  auto full_bar = [&](int i) { return bar0 + 8u * i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (L::STAGES + i); };
+  auto accf_bar = [&](int i) { return bar0 + 8u * (2 * L::STAGES + i); };
+  auto acce_bar = [&](int i) { return bar0 + 8u * (2 * L::STAGES + 2 + i); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * L::STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFFSET);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFFSET + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFFSET + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (blockIdx.x == 0 && a.clear_err && threadIdx.x == 0) *a.err = 0;
+  if (!a.dependent) {
+    if (blockIdx.x == 0)
+      for (int i = threadIdx.x; i < a.zero_count; i += blockDim.x) a.zero_ptr[i] = 0;
+    pdl_launch_dependents();  // the down kernel may begin its prologue
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::STAGES; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(accf_bar(i), 1);
+      mbar_init(acce_bar(i), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int64_t total = (int64_t)a.tiles * a.kb_tile;  // k-blocks of the whole launch
+  const int64_t ctas = gridDim.x;
+  const int64_t x_begin = ng_start(blockIdx.x, total, ctas);
+  const int64_t x_end = ng_start(blockIdx.x + 1, total, ctas);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      // A dependent launch first fills the ring with weights only (they do not
+      // depend on the previous kernel), then waits, then adds the activations.
+      int pending_x = 0;  // ring slots holding weights whose activation load is deferred
+      int32_t pending_k0[L::STAGES];
+      if (a.dependent) {
+        int64_t x = x_begin;
+        while (x < x_end && pending_x < L::STAGES) {
+          const int tile = (int)(x / a.kb_tile);
+          const int k0 = (int)(x - (int64_t)tile * a.kb_tile) * TC_BK;
+          const uint32_t sw = sbase + pending_x * L::STAGE_BYTES;
+          mbar_arrive_expect_tx(full_bar(pending_x), L::STAGE_BYTES);
+          if (GATE_UP)
+            tma_load_3d(sw, &tmW, full_bar(pending_x), k0, tile * TILE_ROWS, 0);
+          else
+            tma_load_2d(sw, &tmW, full_bar(pending_x), k0, tile * TILE_ROWS);
+          pending_k0[pending_x] = k0;
+          issued_mask |= 1u << pending_x;
+          ++pending_x;
+          ++x;
+        }
+        pdl_wait();
+        if (blockIdx.x == 0)
+          for (int i = 0; i < a.zero_count; ++i) a.zero_ptr[i] = 0;
+        for (int i = 0; i < pending_x; ++i)
+          tma_load_2d(sbase + i * L::STAGE_BYTES + L::W_BYTES, &tmX, full_bar(i), pending_k0[i], 0);
+      }
+      int skip = pending_x;  // k-blocks already issued above
+      for (int64_t x = x_begin; x < x_end && ok;) {
+        const int tile = (int)(x / a.kb_tile);
+        const int kb0 = (int)(x - (int64_t)tile * a.kb_tile);
+        const int nkb = (int)min((int64_t)(a.kb_tile - kb0), x_end - x);
+        x += nkb;
+        for (int i = 0; i < nkb; ++i) {
+          if (skip > 0) {
+            --skip;
+            if (++stage == L::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, a.wait_limit_ns, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sw = sbase + stage * L::STAGE_BYTES;
+          const uint32_t sx = sw + L::W_BYTES;
+          const int k0 = (kb0 + i) * TC_BK;
+          mbar_arrive_expect_tx(full_bar(stage), L::STAGE_BYTES);
+          if (GATE_UP)
+            tma_load_3d(sw, &tmW, full_bar(stage), k0, tile * TILE_ROWS, 0);
+          else
+            tma_load_2d(sw, &tmW, full_bar(stage), k0, tile * TILE_ROWS);
+          tma_load_2d(sx, &tmX, full_bar(stage), k0, 0);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == L::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int i = 0; i < L::STAGES; ++i)
+          if (issued_mask & (1u << i))
+            mbar_wait_bounded(full_bar(i), (issued_parity >> i) & 1u, a.wait_limit_ns, nullptr,
+                              a.err);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_f16(BF16, false, false, 128, NT);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int64_t x = x_begin; x < x_end && ok;) {
+        const int tile = (int)(x / a.kb_tile);
+        const int kb0 = (int)(x - (int64_t)tile * a.kb_tile);
+        const int nkb = (int)min((int64_t)(a.kb_tile - kb0), x_end - x);
+        x += nkb;
+        if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, a.wait_limit_ns, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * NT;
+        for (int i = 0; i < nkb; ++i) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, a.wait_limit_ns, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sw = sbase + stage * L::STAGE_BYTES;
+          const uint32_t sx = sw + L::W_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < TC_BK / TC_UMMA_K; ++kk)
+            umma_f16_ss(d_tmem, make_sw128_desc(sw + kk * 32, 16, 1024),
+                        make_sw128_desc(sx + kk * 32, 16, 1024), idesc, (i | kk) != 0 ? 1u : 0u);
+          umma_commit(empty_bar(stage));
+          if (++stage == L::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(accf_bar(acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      umma_commit(drain_bar);
+      mbar_wait_bounded(drain_bar, 0, a.wait_limit_ns, nullptr, a.err);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // weight row of the tile = TMEM lane
+    const int e = threadIdx.x - 64;       // 0..127 among the epilogue threads
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int seg = 0;
+    for (int64_t x = x_begin; x < x_end; ++seg) {
+      const int tile = (int)(x / a.kb_tile);
+      const int kb0 = (int)(x - (int64_t)tile * a.kb_tile);
+      x += min((int64_t)(a.kb_tile - kb0), x_end - x);
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_wait_bounded(accf_bar(acc), acc_phase, a.wait_limit_ns, abort_flag, a.err) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!epi_bar_and(ok)) break;  // all four epilogue warps leave together
+      {
+        tc_fence_after();
+        float* dst = a.part + (((size_t)blockIdx.x * a.seg_max + seg) * 128 + row) * NT;
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * NT;
+#pragma unroll
+        for (int c = 0; c < NT; c += 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(taddr + c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            reinterpret_cast<float4*>(dst + c)[q] =
+                make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                            __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        }
+        tc_fence_before();
+        mbar_arrive(acce_bar(acc));  // accumulator free for the unit after next
+        __threadfence();
+      }
+      // CTAs sharing this tile: owners of its first and last k-block
+      const int c_first = ng_owner((int64_t)tile * a.kb_tile, total, ctas);
+      const int c_last = ng_owner((int64_t)(tile + 1) * a.kb_tile - 1, total, ctas);
+      const int nparts = c_last - c_first + 1;
+      epi_bar_sync();
+      if (e == 0) {
+        int last = 0;
+        if (!*abort_flag) last = atomicAdd(a.counters + tile, 1) == nparts - 1;
+        *last_flag = last;
+      }
+      epi_bar_sync();
+      const int last = *last_flag;
+      if (last) {
+        __threadfence();
+        // partial of CTA c for this tile: its segment index is tile - (first tile of c)
+        auto part_of = [&](int c) -> const float* {
+          const int j = tile - (int)(ng_start(c, total, ctas) / a.kb_tile);
+          return a.part + ((size_t)c * a.seg_max + j) * 128 * NT;
+        };
+        if (GATE_UP) {
+          // thread e: hidden unit tile*64 + (e & 63), tokens [h*NT/2, (h+1)*NT/2)
+          const int jr = e & 63, h = e >> 6;
+          const int j = tile * 64 + jr;
+          float g[NT / 2], uu[NT / 2];
+#pragma unroll
+          for (int n = 0; n < NT / 2; ++n) g[n] = uu[n] = 0.0f;
+          for (int c0 = c_first; c0 <= c_last; c0 += RB) {
+            // issue the loads of up to RB partials, then add them in CTA order
+            float4 vg[RB][NT / 8], vu[RB][NT / 8];
+#pragma unroll
+            for (int q = 0; q < RB; ++q)
+              if (c0 + q <= c_last) {
+                const float* pb = part_of(c0 + q);
+#pragma unroll
+                for (int n = 0; n < NT / 8; ++n) {
+                  vg[q][n] = __ldcg(reinterpret_cast<const float4*>(pb + jr * NT + h * (NT / 2)) + n);
+                  vu[q][n] = __ldcg(reinterpret_cast<const float4*>(pb + (64 + jr) * NT + h * (NT / 2)) + n);
+                }
+              }
+#pragma unroll
+            for (int q = 0; q < RB; ++q)
+              if (c0 + q <= c_last) {
+#pragma unroll
+                for (int n = 0; n < NT / 8; ++n) {
+                  g[4 * n] += vg[q][n].x; g[4 * n + 1] += vg[q][n].y;
+                  g[4 * n + 2] += vg[q][n].z; g[4 * n + 3] += vg[q][n].w;
+                  uu[4 * n] += vu[q][n].x; uu[4 * n + 1] += vu[q][n].y;
+                  uu[4 * n + 2] += vu[q][n].z; uu[4 * n + 3] += vu[q][n].w;
+                }
+              }
+          }
+          if (j < a.rows) {
+#pragma unroll
+            for (int n = 0; n < NT / 2; ++n) {
+              const int m = h * (NT / 2) + n;
+              if (m < a.M) {
+                const float v = silu_f32(g[n]) * uu[n];
+                if (BF16)
+                  reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)m * a.ld_out + j] =
+                      __float2bfloat16_rn(v);
+                else
+                  reinterpret_cast<__half*>(a.out)[(int64_t)m * a.ld_out + j] = __float2half_rn(v);
+              }
+            }
+          }
+        } else {
+          // thread e: output feature tile*128 + e, all tokens
+          const int d = tile * 128 + e;
+          float y[NT];
+#pragma unroll
+          for (int n = 0; n < NT; ++n) y[n] = 0.0f;
+          for (int c0 = c_first; c0 <= c_last; c0 += RB) {
+            float4 v[RB][NT / 4];
+#pragma unroll
+            for (int q = 0; q < RB; ++q)
+              if (c0 + q <= c_last) {
+                const float* pb = part_of(c0 + q) + e * NT;
+#pragma unroll
+                for (int n = 0; n < NT / 4; ++n) v[q][n] = __ldcg(reinterpret_cast<const float4*>(pb) + n);
+              }
+#pragma unroll
+            for (int q = 0; q < RB; ++q)
+              if (c0 + q <= c_last) {
+#pragma unroll
+                for (int n = 0; n < NT / 4; ++n) {
+                  y[4 * n] += v[q][n].x; y[4 * n + 1] += v[q][n].y;
+                  y[4 * n + 2] += v[q][n].z; y[4 * n + 3] += v[q][n].w;
+                }
+              }
+          }
+          if (d < a.rows) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              if (n < a.M) {
+                if (BF16)
+                  reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)n * a.ld_out + d] =
+                      __float2bfloat16_rn(y[n]);
+                else
+                  reinterpret_cast<__half*>(a.out)[(int64_t)n * a.ld_out + d] =
+                      __float2half_rn(y[n]);
+              }
+            }
+          }
+        }
+        if (e == 0) a.counters[tile] = 0;  // ready for the next call
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+}  // namespace swiglu

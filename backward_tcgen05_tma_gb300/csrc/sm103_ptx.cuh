@@ -103,6 +103,19 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Lets the next kernel on the stream (launched with programmatic stream
+// serialization) start its prologue before this grid has finished.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the preceding grid has completed and its memory is visible.
+// A no-op when the kernel was not launched as a dependent.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // tcgen05: tensor memory and the 5th-generation tensor core
 // ---------------------------------------------------------------------------
 // Allocate ncols TMEM columns (power of two, 32..512); the TMEM address is

@@ -20,6 +20,7 @@
 #include <vector>
 
 #include "../../include/swiglu_mlp.h"
+#include "ng_gemm.cuh"
 #include "simt_gemm.cuh"
 #include "tc_gemm.cuh"
 
@@ -32,6 +33,8 @@ constexpr int TC_STAGES = 4;
 constexpr int TC_BN = 256;
 
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+
+swiglu_status cuda_status(cudaError_t e);
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_last_launches{0};
 
@@ -40,12 +43,13 @@ std::atomic<int> g_last_launches{0};
 // ---------------------------------------------------------------------------
 enum KernelId : int {
   K_GATE_UP = 0, K_DOWN, K_DGU, K_DWD, K_DWGU, K_DX, K_GATE_UP_NOGRAD, K_DOWN_NOGRAD,
-  K_SIMT_GATE_UP, K_SIMT_DOWN, K_SIMT_DGU, K_SIMT_DWD, K_SIMT_DWGU, K_SIMT_DX, K_COUNT
+  K_SIMT_GATE_UP, K_SIMT_DOWN, K_SIMT_DGU, K_SIMT_DWD, K_SIMT_DWGU, K_SIMT_DX, K_NG_GATE_UP,
+  K_NG_DOWN, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
     "gate_up_swiglu", "down_proj", "dgu_inplace", "dwd", "dwgu", "dx", "gate_up_nograd",
     "down_proj_nograd", "simt_gate_up_swiglu", "simt_down_proj", "simt_dgu_inplace", "simt_dwd",
-    "simt_dwgu", "simt_dx"};
+    "simt_dwgu", "simt_dx", "nograd_small_gate_up", "nograd_small_down"};
 
 struct ProfRec {
   int id;
@@ -199,6 +203,119 @@ cudaError_t launch_simt(int kid, SimtOperand A, SimtOperand B, SimtOperand B2, i
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// no-grad forward for M <= 64 tokens: split-contraction swap-AB kernels
+// ---------------------------------------------------------------------------
+constexpr int NG_MAX_M = 64;
+constexpr int NG_MAX_CTAS = 256;  // stream-K CTAs per launch (one per SM, capped)
+
+struct NgPlan {
+  int NT;
+  int t1, kb1;  // gate/up: tiles of 64 hidden units, k-blocks over D
+  int t2, kb2;  // down: tiles of 128 output features, k-blocks over H
+  size_t counter_bytes, part_bytes;
+};
+
+bool ng_eligible(int64_t M, int64_t D, int64_t H, swiglu_dtype dt) {
+  return dt != SWIGLU_F32_IEEE && M >= 1 && M <= NG_MAX_M;
+}
+
+// A CTA's range of ceil(total / ctas) k-blocks meets at most
+// ceil(range / kb) + 1 tiles, so ctas x seg_max <= tiles + 3 ctas partial
+// slots for any grid up to NG_MAX_CTAS: the workspace bound below does not
+// depend on the device.
+NgPlan ng_plan(int64_t M, int64_t D, int64_t H) {
+  NgPlan p;
+  p.NT = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+  p.t1 = (int)((H + 63) / 64);
+  p.kb1 = (int)((D + 63) / 64);
+  p.t2 = (int)((D + 127) / 128);
+  p.kb2 = (int)((H + 63) / 64);
+  p.counter_bytes = (((size_t)(p.t1 + p.t2) * 4 + 255) / 256) * 256;
+  const size_t slots = (size_t)(p.t1 > p.t2 ? p.t1 : p.t2) + 3 * NG_MAX_CTAS;
+  p.part_bytes = slots * 128 * p.NT * 4;
+  return p;
+}
+
+void ng_grid(int tiles, int kb, int& ctas, int& seg_max) {
+  const int64_t total = (int64_t)tiles * kb;
+  int nsm = sm_count();
+  if (nsm < 1) nsm = 1;
+  int64_t c = nsm < NG_MAX_CTAS ? nsm : NG_MAX_CTAS;
+  if (c > total) c = total;
+  ctas = (int)c;
+  const int64_t range = (total + c - 1) / c;
+  seg_max = (int)((range + kb - 1) / kb) + 1;
+}
+
+template <int NT, bool GATE_UP, bool BF16>
+cudaError_t launch_ng(int kid, const CUtensorMap& tw, const CUtensorMap& tx, NgArgs a,
+                      cudaStream_t st) {
+  auto kern = ng_gemm_kernel<NT, GATE_UP, BF16>;
+  constexpr int smem = NgSmem<NT>::DYN_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int grid = 1;
+  ng_grid(a.tiles, a.kb_tile, grid, a.seg_max);
+  ProfScope prof(kid, st);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  // the down kernel overlaps its prologue and weight prefetch with gate/up's tail
+  // (per-kernel event timing would serialise the two, so it is not used then)
+  const bool pdl = a.dependent && !g_prof_on.load();
+  if (!pdl) a.dependent = 0;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, tw, tx, a);
+  g_last_launches.fetch_add(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// ws layout: [0, 256) header (error word at 0); per-tile counters of the
+// gate/up kernel then of the down kernel; fp32 partial tiles.  The counters
+// must be zero when a call starts: each kernel zeroes the other's counters
+// at its start and every tile's reducer zeroes its own, so a zero-filled
+// workspace stays valid across calls.
+template <int NT, bool BF16>
+swiglu_status ng_forward_nt(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
+                            int64_t M, int64_t D, int64_t H, const NgPlan& p, char* ws,
+                            cudaStream_t st) {
+  int* err = reinterpret_cast<int*>(ws);
+  int* counters = reinterpret_cast<int*>(ws + WS_HEADER);
+  float* part = reinterpret_cast<float*>(ws + WS_HEADER + p.counter_bytes);
+  const uint64_t wl = g_wait_limit_ns.load();
+  CUtensorMap tw, tx;
+  if (!encode_gateup(&tw, BF16, Wgu, D, H, 64) || !map_kmajor(&tx, BF16, X, D, M, D, NT))
+    return SWIGLU_ERR_CUDA;
+  NgArgs a1{(int)M, (int)H, p.kb1, p.t1, 0, part, counters, counters + p.t1, p.t2, 1, 0,
+            A, H, wl, err};
+  if (launch_ng<NT, true, BF16>(K_NG_GATE_UP, tw, tx, a1, st) != cudaSuccess)
+    return SWIGLU_ERR_CUDA;
+  if (!map_kmajor(&tw, BF16, Wd, H, D, H, 128) || !map_kmajor(&tx, BF16, A, H, M, H, NT))
+    return SWIGLU_ERR_CUDA;
+  NgArgs a2{(int)M, (int)D, p.kb2, p.t2, 0, part, counters + p.t1, counters, p.t1, 0, 1,
+            Y, D, wl, err};
+  return cuda_status(launch_ng<NT, false, BF16>(K_NG_DOWN, tw, tx, a2, st));
+}
+
+template <bool BF16>
+swiglu_status ng_forward(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
+                         int64_t M, int64_t D, int64_t H, char* ws, cudaStream_t st) {
+  const NgPlan p = ng_plan(M, D, H);
+  switch (p.NT) {
+    case 16: return ng_forward_nt<16, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, st);
+    case 32: return ng_forward_nt<32, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, st);
+    default: return ng_forward_nt<64, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, st);
+  }
+}
+
 size_t elt_bytes(swiglu_dtype dt) {
   switch (dt) {
     case SWIGLU_BF16:
@@ -234,7 +351,9 @@ swiglu_status check_ptrs(std::initializer_list<const void*> ps) {
   return SWIGLU_OK;
 }
 
-swiglu_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA; }
+swiglu_status cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
 
 // ---------------------------------------------------------------------------
 // tensor-core (bf16 / fp16) paths
@@ -365,11 +484,10 @@ size_t swiglu_mlp_saved_bytes(int64_t M, int64_t H, swiglu_dtype dtype) {
 }
 
 size_t swiglu_mlp_workspace_bytes(int64_t M, int64_t D, int64_t H, swiglu_dtype dtype, int op) {
-  (void)M;
-  (void)D;
-  (void)H;
-  (void)dtype;
-  (void)op;
+  if (op == SWIGLU_OP_FWD_NOGRAD && D > 0 && H > 0 && ng_eligible(M, D, H, dtype)) {
+    const NgPlan p = ng_plan(M, D, H);
+    return WS_HEADER + p.counter_bytes + p.part_bytes;
+  }
   return WS_HEADER;
 }
 
@@ -409,6 +527,11 @@ swiglu_status swiglu_mlp_fwd_nograd(const void* X, const void* Wgu, const void* 
   if (M == 0) return SWIGLU_OK;
   if ((st = check_ptrs({X, Wgu, Wd, Y, A})) != SWIGLU_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (ng_eligible(M, D, H, dtype)) {
+    char* w = static_cast<char*>(ws);
+    return dtype == SWIGLU_BF16 ? ng_forward<true>(X, Wgu, Wd, Y, A, M, D, H, w, s)
+                                : ng_forward<false>(X, Wgu, Wd, Y, A, M, D, H, w, s);
+  }
   int* err = static_cast<int*>(ws);
   if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
   switch (dtype) {

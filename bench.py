@@ -276,14 +276,16 @@ def _e2e(api, t, o, steps):
     return e0.elapsed_time(e1) / 1e3 / steps, h2d, d2h
 
 
-def _nograd_sweep(api, device, peaks):
+def _nograd_sweep(api, device, peaks, sizes=NOGRAD_S):
     import torch
     from backward_tcgen05_tma_gb300 import metrics, synthetic
     D, H = 4096, 11008
-    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)  # 512 MiB > L2
+    # L2 flush by READING 512 MiB (> 129 MB L2): a write-based flush would leave
+    # dirty lines whose write-back lands inside the timed call
+    flush = torch.ones(128 * 2 ** 20, dtype=torch.float32, device=device)
     wts = synthetic.make_inputs(1, D, H, "bf16", seed=1, device=device, kind="device")
     res = []
-    for S in NOGRAD_S:
+    for S in sizes:
         X = synthetic.device_normal((S, D), 1.0, "bf16", 1, 0, device)
         Y = torch.empty(S, D, dtype=torch.bfloat16, device=device)
         A = torch.empty(S, H, dtype=torch.bfloat16, device=device)
@@ -293,20 +295,27 @@ def _nograd_sweep(api, device, peaks):
             api.swiglu_mlp_fwd_nograd(X, wts["Wgu"], wts["Wd"], out=o, ws=ws)
         times = []
         st = torch.cuda.current_stream()
-        for _ in range(20):
-            flush.zero_()
+        api.swiglu_mlp_profile_read()
+        for it in range(40):
+            flush.sum()
+            if it == 20:  # second half: per-kernel events too
+                api.swiglu_mlp_profile_enable(True)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(st)
             api.swiglu_mlp_fwd_nograd(X, wts["Wgu"], wts["Wd"], out=o, ws=ws)
             e1.record(st)
             e1.synchronize()
-            times.append(e0.elapsed_time(e1) / 1e3)
+            if it < 20:
+                times.append(e0.elapsed_time(e1) / 1e3)
+        api.swiglu_mlp_profile_enable(False)
+        kern = {k: round(v[1] / v[0] * 1e3, 2) for k, v in api.swiglu_mlp_profile_read().items()}
         tmed = statistics.median(times)
         byts = metrics.nograd_algorithmic_bytes(S, D, H)
         res.append({"S": S, "us": round(tmed * 1e6, 2), "GBps": round(byts / tmed / 1e9, 1),
                     "hbm_frac": round(byts / tmed / 1e9 / peaks["hbm_gbs"], 4),
-                    "TFLOPS": round(metrics.fwd_flops(S, D, H) / tmed / 1e12, 2)})
-    return {"workload": "B1_D4096_H11008_bf16_nograd", "l2": "flushed (512 MiB write) before "
+                    "TFLOPS": round(metrics.fwd_flops(S, D, H) / tmed / 1e12, 2),
+                    "kernel_us": kern})
+    return {"workload": "B1_D4096_H11008_bf16_nograd", "l2": "flushed (512 MiB read) before "
             "each timed call", "median_of": 20, "sweep": res}
 
 
@@ -327,6 +336,19 @@ def _cpu_baseline(t_dev, w):
             "cores": oracle.num_threads(), "kind": "oracle",
             "sample": "fwd+bwd of %d token rows (full D=%d, H=%d weights) of the workload, "
                       "fp64 loops, %.1f s" % (m, D, H, dt)}
+
+
+def run_nograd_only(args):
+    """Only the no-grad sweep at the listed sizes (one JSON line)."""
+    import torch
+    from backward_tcgen05_tma_gb300 import api, build
+    torch.cuda.set_device(0)
+    build.build()
+    api.lib()
+    sizes = [int(x) for x in args.nograd.split(",")]
+    out = _nograd_sweep(api, "cuda:0", _peaks(), sizes)
+    print(json.dumps({"metric": "SwiGLU MLP no-grad forward, HBM GB/s", "nograd": out}), flush=True)
+    return 0
 
 
 def run_ours(args):
@@ -434,11 +456,15 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=MAIN)
     ap.add_argument("--quick", action="store_true", help="main workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--nograd", default=None,
+                    help="comma-separated S values: run only the no-grad sweep (B=1, D=4096, H=11008)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.nograd:
+        return run_nograd_only(args)
     return run_ours(args)
 
 

@@ -40,9 +40,12 @@
  * nothing.  ``stream`` is a cudaStream_t (0 = legacy default stream).
  *
  * Workspace: ``ws`` is a device buffer of at least swiglu_mlp_workspace_bytes()
- * bytes, owned by the caller; the library keeps a device error word in it and
- * clears it at the start of every call.  The library itself allocates no
- * memory.
+ * bytes, owned by the caller, ZERO-FILLED before its first use.  The library
+ * keeps a device error word in it (cleared at the start of every call) and,
+ * for the few-token no-grad path, per-tile counters (left at zero by every
+ * completed call) and fp32 partial sums.  After a SWIGLU_ERR_DEVICE_TIMEOUT,
+ * zero-fill it again before reuse.  Calls that share one workspace must not
+ * overlap on the GPU.  The library itself allocates no memory.
  *
  * Calls are asynchronous on ``stream`` and do not synchronise (except
  * swiglu_mlp_query_error).  Argument errors are detected on the host before

@@ -68,7 +68,8 @@ def test_argument_errors_are_reported_before_any_launch(L):
     assert _fwd(L, ws=N) == WSERR
     assert _fwd(L, wsb=8) == WSERR
     assert _fwd(L, M=2 ** 31) == UNSUP
-    assert L.swiglu_mlp_fwd_nograd(N, P, P, P, P, 4, 64, 128, 0, P, 256, N) == INVALID
+    assert L.swiglu_mlp_fwd_nograd(N, P, P, P, P, 4, 64, 128, 0, P, 1 << 30, N) == INVALID
+    assert L.swiglu_mlp_fwd_nograd(P, P, P, P, P, 4, 64, 128, 0, P, 256, N) == WSERR
     assert L.swiglu_mlp_bwd(P, P, P, P, P, P, P, N, 4, 64, 128, 0, P, 256, N) == INVALID
     assert L.swiglu_mlp_bwd(P, P, P, P, P, P, P, P_MIS, 4, 64, 128, 0, P, 256, N) == ALIGN
 
