@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.swiglu_mlp_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
         L.swiglu_mlp_fwd_nograd.restype = ci
         L.swiglu_mlp_fwd_nograd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
+        L.swiglu_mlp_fwd_nograd_noalloc.restype = ci
+        L.swiglu_mlp_fwd_nograd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
         L.swiglu_mlp_bwd.restype = ci
         L.swiglu_mlp_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
         L.swiglu_mlp_query_error.restype = ci
@@ -163,6 +165,21 @@ def swiglu_mlp_fwd_nograd(X, Wgu, Wd, out: dict | None = None, ws=None):
                                        dtype_code(X.dtype), _ptr(ws), ws.numel(),
                                        _stream(X.device)),
            "swiglu_mlp_fwd_nograd")
+    return Y, A
+
+
+def swiglu_mlp_fwd_nograd_noalloc(X, Wgu, Wd, out: dict | None = None):
+    """Few-token no-grad forward that allocates nothing in the library (its
+    scratch is a static device array): returns (Y [M,D], A [M,H])."""
+    M, D, H = _dims(X, Wgu, Wd)
+    out = out or {}
+    Y = out.get("Y")
+    Y = torch.empty(M, D, dtype=X.dtype, device=X.device) if Y is None else Y
+    A = out.get("A")
+    A = torch.empty(M, H, dtype=X.dtype, device=X.device) if A is None else A
+    _check(lib().swiglu_mlp_fwd_nograd_noalloc(_ptr(X), _ptr(Wgu), _ptr(Wd), _ptr(Y), _ptr(A), M,
+                                               D, H, dtype_code(X.dtype), _stream(X.device)),
+           "swiglu_mlp_fwd_nograd_noalloc")
     return Y, A
 
 

@@ -316,6 +316,46 @@ swiglu_status ng_forward(const void* X, const void* Wgu, const void* Wd, void* Y
   }
 }
 
+// ---------------------------------------------------------------------------
+// the same few-token no-grad forward with its scratch in a static device array
+// ---------------------------------------------------------------------------
+// Scratch (error word, tile counters, fp32 partial tiles) for callers that
+// cannot allocate.  It is part of the module image: every GPU that loads this
+// library holds these bytes until the process exits.
+constexpr size_t NOALLOC_SCRATCH_BYTES = 8u << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[NOALLOC_MAX_DEVICES];  // device address of the array, per device
+
+// Host code cannot use g_noalloc_scratch's name as a device address (it is a
+// host-side shadow); the device address is looked up once per device, with
+// that device current, and cached.
+swiglu_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SWIGLU_ERR_CUDA;
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return SWIGLU_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> g(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return SWIGLU_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SWIGLU_OK;
+}
+
+// Scratch bytes one call needs on the current device (its actual grids).
+size_t noalloc_bytes_needed(const NgPlan& p) {
+  int c1 = 1, s1 = 1, c2 = 1, s2 = 1;
+  ng_grid(p.t1, p.kb1, c1, s1);
+  ng_grid(p.t2, p.kb2, c2, s2);
+  const size_t slots1 = (size_t)c1 * s1, slots2 = (size_t)c2 * s2;
+  return WS_HEADER + p.counter_bytes + (slots1 > slots2 ? slots1 : slots2) * 128 * p.NT * 4;
+}
+
 size_t elt_bytes(swiglu_dtype dt) {
   switch (dt) {
     case SWIGLU_BF16:
@@ -543,6 +583,31 @@ swiglu_status swiglu_mlp_fwd_nograd(const void* X, const void* Wgu, const void* 
       return simt_forward((const float*)X, (const float*)Wgu, (const float*)Wd, (float*)Y,
                           nullptr, nullptr, 0, (float*)A, H, M, D, H, s);
   }
+}
+
+swiglu_status swiglu_mlp_fwd_nograd_noalloc(const void* X, const void* Wgu, const void* Wd,
+                                            void* Y, void* A, int64_t M, int64_t D, int64_t H,
+                                            swiglu_dtype dtype, void* stream) {
+  g_last_launches.store(0);
+  if (dtype != SWIGLU_BF16 && dtype != SWIGLU_F16) return SWIGLU_ERR_UNSUPPORTED;
+  if (M < 0 || D <= 0 || H <= 0) return SWIGLU_ERR_INVALID_ARG;
+  if (D % 8 != 0 || H % 8 != 0) return SWIGLU_ERR_ALIGNMENT;
+  if (M > NG_MAX_M || D > 0x7fffffffLL || 3 * H > 0x7fffffffLL) return SWIGLU_ERR_UNSUPPORTED;
+  if (M == 0) return SWIGLU_OK;
+  swiglu_status st = check_ptrs({X, Wgu, Wd, Y, A});
+  if (st != SWIGLU_OK) return st;
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != SWIGLU_OK) return st;
+  const NgPlan p = ng_plan(M, D, H);
+  if (noalloc_bytes_needed(p) > NOALLOC_SCRATCH_BYTES) return SWIGLU_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: clear the error word and
+  // the tile counters, which must start at zero
+  if (cudaMemsetAsync(scratch, 0, WS_HEADER + p.counter_bytes, s) != cudaSuccess)
+    return SWIGLU_ERR_CUDA;
+  char* w = static_cast<char*>(scratch);
+  return dtype == SWIGLU_BF16 ? ng_forward<true>(X, Wgu, Wd, Y, A, M, D, H, w, s)
+                              : ng_forward<false>(X, Wgu, Wd, Y, A, M, D, H, w, s);
 }
 
 swiglu_status swiglu_mlp_bwd(const void* dY, const void* X, const void* Wgu, const void* Wd,

@@ -109,6 +109,36 @@ swiglu_status swiglu_mlp_fwd_nograd(const void* X, const void* Wgu, const void* 
                                     void* A, int64_t M, int64_t D, int64_t H,
                                     swiglu_dtype dtype, void* ws, size_t ws_bytes, void* stream);
 
+/* The few-token no-grad forward (same kernels and results as
+ * swiglu_mlp_fwd_nograd for M <= 64) for callers that cannot allocate device
+ * memory: code that runs while a CUDA graph is being captured, a plug-in
+ * whose host framework owns every device allocation and offers no workspace,
+ * or a latency-critical decode loop that may not call cudaMalloc.  The pages
+ * have no counterpart: it is an interface convenience of this library.
+ *
+ * The caller passes inputs and outputs as in swiglu_mlp_fwd_nograd; there is
+ * no workspace argument.  Scratch (error word, per-tile counters, fp32
+ * partial sums) lives in one file-scope static device array of 8 MiB, which
+ * every GPU that loads this library holds until the process exits.  The call
+ * allocates nothing (no cudaMalloc/cudaFree, no allocating library routine).
+ *
+ * Limits: bf16/fp16 only, 0 <= M <= 64, D and H multiples of 8, and the
+ * partial sums of the call must fit the array (for D = 4096, H = 11008 on a
+ * 152-SM GB300: M <= 32); anything beyond returns SWIGLU_ERR_UNSUPPORTED
+ * without launching.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  Every call clears the error word
+ * and counters in the array (an asynchronous memset, no allocation) and then
+ * launches the two kernels.  All calls share the one array: calls that
+ * overlap on the GPU (other streams, other threads) race and give undefined
+ * results.  Device errors are not reported through a workspace; use
+ * swiglu_mlp_fwd_nograd when they must be queried. */
+swiglu_status swiglu_mlp_fwd_nograd_noalloc(const void* X, const void* Wgu, const void* Wd,
+                                            void* Y, void* A, int64_t M, int64_t D, int64_t H,
+                                            swiglu_dtype dtype, void* stream);
+
 /* Backward.  Consumes ``saved`` as written by swiglu_mlp_fwd on the same
  * X, Wgu, Wd: the expired G/U columns are overwritten in place with dG/dU
  * ("Summary": overwrite expired G/U storage with dG/dU; "Known limitations":

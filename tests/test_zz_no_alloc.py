@@ -1,0 +1,67 @@
+"""The no-allocation no-grad forward (swiglu_mlp_fwd_nograd_noalloc).
+
+Some callers cannot allocate device memory -- code running under CUDA-graph
+capture, plug-ins whose host framework owns all device memory, decode loops
+that must not call cudaMalloc -- so this entry point takes no workspace and
+keeps its scratch in a static device array inside the library.  This file
+checks, through the C ABI, that two calls in a row give the same outputs as
+the workspace entry point (within the parity tolerance), and that shapes
+beyond the array's limit are refused without a launch.  It is collected last
+so that a failure here never hides the other tests' results."""
+import ctypes
+
+import pytest
+import torch
+
+from backward_tcgen05_tma_gb300 import api, build, synthetic
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2  # relative Frobenius tolerance of the bf16/fp16 parity tests
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    return api.lib()
+
+
+def _rel(got, ref):
+    g, r = got.double(), ref.double()
+    return float((g - r).norm() / r.norm().clamp_min(1e-30))
+
+
+def _noalloc(L, t, M, D, H, dt):
+    Y = torch.empty(M, D, dtype=t["X"].dtype, device="cuda")
+    A = torch.empty(M, H, dtype=t["X"].dtype, device="cuda")
+    rc = L.swiglu_mlp_fwd_nograd_noalloc(
+        ctypes.c_void_p(t["X"].data_ptr()), ctypes.c_void_p(t["Wgu"].data_ptr()),
+        ctypes.c_void_p(t["Wd"].data_ptr()), ctypes.c_void_p(Y.data_ptr()),
+        ctypes.c_void_p(A.data_ptr()), M, D, H, dt,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    return rc, Y, A
+
+
+@pytest.mark.parametrize("dtn,M,D,H", [("bf16", 1, 4096, 11008), ("bf16", 16, 4096, 11008),
+                                       ("f16", 5, 320, 392), ("bf16", 32, 512, 1024)])
+def test_noalloc_matches_workspace_entry_point(L, dtn, M, D, H):
+    dt = {"bf16": 0, "f16": 1}[dtn]
+    t = synthetic.make_inputs(M, D, H, dtn, seed=M, device="cuda", kind="device")
+    Y_ref, A_ref = api.swiglu_mlp_fwd_nograd(t["X"], t["Wgu"], t["Wd"])
+    for _ in range(2):  # the array keeps the previous call's contents
+        rc, Y, A = _noalloc(L, t, M, D, H, dt)
+        assert rc == 0, api.status_string(rc)
+        torch.cuda.synchronize()
+        assert _rel(Y, Y_ref) <= TOL
+        assert _rel(A, A_ref) <= TOL
+
+
+def test_noalloc_rejects_sizes_beyond_its_array(L):
+    t = synthetic.make_inputs(64, 4096, 11008, "bf16", seed=1, device="cuda", kind="device")
+    rc, _, _ = _noalloc(L, t, 64, 4096, 11008, 0)   # partial sums exceed the 8 MiB array
+    assert rc == 3 and L.swiglu_mlp_last_launch_count() == 0
+    t = synthetic.make_inputs(65, 64, 128, "bf16", seed=1, device="cuda")
+    rc, _, _ = _noalloc(L, t, 65, 64, 128, 0)      # more tokens than the path serves
+    assert rc == 3 and L.swiglu_mlp_last_launch_count() == 0
