@@ -90,8 +90,10 @@ __device__ __forceinline__ int epi_bar_and(int v) {
   return r;
 }
 
+constexpr int NG_THREADS = 192;  // producer warp, MMA warp, 4 epilogue warps
+
 template <int NT, bool GATE_UP, bool BF16>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+__global__ void __launch_bounds__(NG_THREADS, 1)
     ng_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const NgArgs a) {
   using L = NgSmem<NT>;

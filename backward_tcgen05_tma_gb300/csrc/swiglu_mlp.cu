@@ -260,7 +260,7 @@ cudaError_t launch_ng(int kid, const CUtensorMap& tw, const CUtensorMap& tx, NgA
   ProfScope prof(kid, st);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(TC_THREADS);
+  cfg.blockDim = dim3(NG_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];

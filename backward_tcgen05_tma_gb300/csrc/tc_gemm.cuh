@@ -8,10 +8,12 @@
 // or N contiguous); the tensor core reads both layouts natively, so no
 // operand of the MLP's six GEMMs is ever transposed in memory.
 //
-// CTA = 6 warps, one CTA per SM, persistent over output tiles:
+// CTA = 10 warps, one CTA per SM, persistent over output tiles:
 //   warp 0      TMA producer: fills a STAGES-deep ring of (A, B) k-blocks
 //   warp 1      owns TMEM (allocates 2 x BN columns) and issues tcgen05.mma
-//   warps 2..5  epilogue: TMEM -> registers -> fused elementwise -> global
+//   warps 2..9  epilogue: TMEM -> registers -> fused elementwise -> global;
+//               warps w and w + 4 share TMEM lane quarter (w % 4) and split
+//               the tile's columns in two halves
 // Two TMEM accumulators alternate between tiles, so the epilogue of tile i
 // overlaps the main loop of tile i + 1.  Every wait is bounded (see
 // mbar_wait_bounded); a stuck pipeline records an error and the CTA unwinds.
@@ -26,7 +28,8 @@ namespace swiglu {
 
 constexpr int TC_BM = 128;       // tile rows (MMA M)
 constexpr int TC_BK = 64;        // k-block: 64 16-bit elements = one 128-byte swizzle row
-constexpr int TC_THREADS = 192;  // 6 warps
+constexpr int TC_THREADS = 320;  // 10 warps
+constexpr int TC_EPI_THREADS = 256;  // warps 2..9
 constexpr int TC_UMMA_K = 16;    // K of one kind::f16 MMA
 
 enum LoadMode : int {
@@ -58,10 +61,10 @@ __device__ __forceinline__ void tc_tile_coords(int t, const TcShape& s, int& mt,
 }
 
 // ---------------------------------------------------------------------------
-// Epilogues.  Each is called by the 128 epilogue threads of a CTA for one
+// Epilogues.  Each is called by the 256 epilogue threads of a CTA for one
 // output tile; thread `row` (0..127) owns output row m0 + row and reads its
-// TMEM lane.  `tacc` is the TMEM address of this warp's lane quarter at the
-// accumulator's first column.
+// TMEM lane, over column half `half` (0 or 1) of the tile.  `tacc` is the
+// TMEM address of this warp's lane quarter at the accumulator's first column.
 // ---------------------------------------------------------------------------
 template <bool BF16>
 struct Pack;
@@ -101,13 +104,13 @@ struct EpiStore {
   };
   template <int BN, bool BF16>
   static __device__ __forceinline__ void run(const Params& p, const TcShape& s, uint32_t tacc,
-                                             int m0, int nt, int row) {
+                                             int m0, int nt, int row, int half) {
     using P = Pack<BF16>;
     const int m = m0 + row;
     const int n0 = nt * BN;
     typename P::T* out = reinterpret_cast<typename P::T*>(p.out) + (int64_t)m * p.ld;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(tacc + c * 32, r);
       tmem_ld_wait();
@@ -143,7 +146,7 @@ struct EpiSwiGLU {
   };
   template <int BN, bool BF16>
   static __device__ __forceinline__ void run(const Params& p, const TcShape& s, uint32_t tacc,
-                                             int m0, int nt, int row) {
+                                             int m0, int nt, int row, int half) {
     using P = Pack<BF16>;
     using T = typename P::T;
     constexpr int HALF = BN / 2;
@@ -151,7 +154,7 @@ struct EpiSwiGLU {
     const int j0 = nt * HALF;
     const bool keep_gu = p.g != nullptr;
 #pragma unroll 1
-    for (int c = 0; c < HALF / 32; ++c) {
+    for (int c = half * (HALF / 64); c < (half + 1) * (HALF / 64); ++c) {
       uint32_t rg[32], ru[32];
       tmem_ld_32x32b_x32(tacc + c * 32, rg);
       tmem_ld_32x32b_x32(tacc + HALF + c * 32, ru);
@@ -197,29 +200,58 @@ struct EpiDSwiGLU {
     void* u;
     int64_t ld;
   };
+  // G and U of one 32-column chunk of this thread's row (zero outside the
+  // matrix), loaded a chunk ahead so their latency hides behind the math.
+  template <bool BF16>
+  static __device__ __forceinline__ void load_gu(const Params& p, const TcShape& s, int m, int j0,
+                                                 uint4 (&vg)[4], uint4 (&vu)[4]) {
+    using T = typename Pack<BF16>::T;
+    const T* grow = reinterpret_cast<const T*>(p.g) + (int64_t)m * p.ld;
+    const T* urow = reinterpret_cast<const T*>(p.u) + (int64_t)m * p.ld;
+#pragma unroll
+    for (int g8 = 0; g8 < 4; ++g8) {
+      const int j = j0 + g8 * 8;
+      if (m < s.M && j + 8 <= s.N) {
+        vg[g8] = *reinterpret_cast<const uint4*>(grow + j);
+        vu[g8] = *reinterpret_cast<const uint4*>(urow + j);
+      } else {
+        vg[g8] = make_uint4(0, 0, 0, 0);
+        vu[g8] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
   template <int BN, bool BF16>
   static __device__ __forceinline__ void run(const Params& p, const TcShape& s, uint32_t tacc,
-                                             int m0, int nt, int row) {
+                                             int m0, int nt, int row, int half) {
     using P = Pack<BF16>;
     using T = typename P::T;
     const int m = m0 + row;
-    const int j0 = nt * BN;
+    const int jt = nt * BN;
+    constexpr int CH = BN / 64;  // chunks of 32 columns per half
+    const int c0 = half * CH;
     T* grow = reinterpret_cast<T*>(p.g) + (int64_t)m * p.ld;
     T* urow = reinterpret_cast<T*>(p.u) + (int64_t)m * p.ld;
+    uint4 ng[4], nu[4];
+    load_gu<BF16>(p, s, m, jt + c0 * 32, ng, nu);
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = c0; c < c0 + CH; ++c) {
+      uint4 vg[4], vu[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        vg[q] = ng[q];
+        vu[q] = nu[q];
+      }
+      if (c + 1 < c0 + CH) load_gu<BF16>(p, s, m, jt + (c + 1) * 32, ng, nu);
       uint32_t r[32];
       tmem_ld_32x32b_x32(tacc + c * 32, r);
       tmem_ld_wait();
       if (m < s.M) {
 #pragma unroll
         for (int g8 = 0; g8 < 4; ++g8) {
-          const int j = j0 + c * 32 + g8 * 8;
+          const int j = jt + c * 32 + g8 * 8;
           if (j + 8 <= s.N) {
-            const uint4 vg = *reinterpret_cast<const uint4*>(grow + j);
-            const uint4 vu = *reinterpret_cast<const uint4*>(urow + j);
-            const uint32_t* pg = &vg.x;
-            const uint32_t* pu = &vu.x;
+            const uint32_t* pg = &vg[g8].x;
+            const uint32_t* pu = &vu[g8].x;
             uint4 og, ou;
             uint32_t* qg = &og.x;
             uint32_t* qu = &ou.x;
@@ -297,7 +329,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(accf_bar(i), 1);
-      mbar_init(acce_bar(i), 128);
+      mbar_init(acce_bar(i), TC_EPI_THREADS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -430,6 +462,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // column half of the tile
     const int row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -444,7 +477,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int mt, nt;
       tc_tile_coords(t, s, mt, nt);
       const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      Epi::template run<BN, BF16>(ep, s, tacc, mt * TC_BM, nt, row);
+      Epi::template run<BN, BF16>(ep, s, tacc, mt * TC_BM, nt, row, half);
       tc_fence_before();
       mbar_arrive(acce_bar(acc));
       if (++acc == 2) {
