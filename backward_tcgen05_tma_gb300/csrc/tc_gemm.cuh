@@ -93,6 +93,39 @@ struct Pack<false> {
   }
 };
 
+// Coalesced store of one 32 x 32 tile of 16-bit values held row-per-thread
+// (lane l owns row l: 16 packed words = 64 bytes).  The warp transposes it
+// through a 2 KB shared buffer and then writes 8 rows x 64 contiguous bytes
+// per instruction, so every 32-byte sector is written whole (row-per-thread
+// 16-byte stores leave sectors half-written and cost read-modify-write
+// traffic).  The buffer's 16-byte chunks are XOR-swizzled by (row / 2) % 4,
+// which keeps both the row writes and the column reads free of bank
+// conflicts.  row_ptr(r) is row r's destination for this chunk (or nullptr
+// when the row is outside the matrix); chunk_ok(q) says whether 8-column
+// group q lies inside it.
+template <class RowPtr, class ChunkOk>
+__device__ __forceinline__ void warp_store_tile(uint8_t* buf, const uint32_t (&v)[16], int lane,
+                                                RowPtr row_ptr, ChunkOk chunk_ok) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int pc = c ^ ((lane >> 1) & 3);
+    *reinterpret_cast<uint4*>(buf + lane * 64 + pc * 16) =
+        make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+  }
+  __syncwarp();
+  const int q = lane & 3;
+  const bool qok = chunk_ok(q);
+#pragma unroll
+  for (int pass = 0; pass < 4; ++pass) {
+    const int r = pass * 8 + (lane >> 2);
+    const int pc = q ^ ((r >> 1) & 3);
+    const uint4 w = *reinterpret_cast<const uint4*>(buf + r * 64 + pc * 16);
+    uint8_t* dst = row_ptr(r);
+    if (dst != nullptr && qok) *reinterpret_cast<uint4*>(dst + q * 16) = w;
+  }
+  __syncwarp();
+}
+
 // SiLU(g) = g / (1 + e^-g), evaluated in fp32.
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + __expf(-g)); }
 
@@ -104,30 +137,30 @@ struct EpiStore {
   };
   template <int BN, bool BF16>
   static __device__ __forceinline__ void run(const Params& p, const TcShape& s, uint32_t tacc,
-                                             int m0, int nt, int row, int half) {
+                                             int m0, int nt, int row, int half, uint8_t* buf) {
     using P = Pack<BF16>;
-    const int m = m0 + row;
+    using T = typename P::T;
+    const int lane = row & 31;
+    const int mw = m0 + (row & ~31);  // first row of this warp's 32
     const int n0 = nt * BN;
-    typename P::T* out = reinterpret_cast<typename P::T*>(p.out) + (int64_t)m * p.ld;
 #pragma unroll 1
     for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(tacc + c * 32, r);
       tmem_ld_wait();
-      if (m < s.M) {
+      uint32_t v[16];
 #pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) {
-          const int n = n0 + c * 32 + g8 * 8;
-          if (n + 8 <= s.N) {
-            uint4 v;
-            v.x = P::two(__uint_as_float(r[g8 * 8 + 0]), __uint_as_float(r[g8 * 8 + 1]));
-            v.y = P::two(__uint_as_float(r[g8 * 8 + 2]), __uint_as_float(r[g8 * 8 + 3]));
-            v.z = P::two(__uint_as_float(r[g8 * 8 + 4]), __uint_as_float(r[g8 * 8 + 5]));
-            v.w = P::two(__uint_as_float(r[g8 * 8 + 6]), __uint_as_float(r[g8 * 8 + 7]));
-            *reinterpret_cast<uint4*>(out + n) = v;
-          }
-        }
-      }
+      for (int i = 0; i < 16; ++i) v[i] = P::two(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+      const int nc = n0 + c * 32;
+      warp_store_tile(
+          buf, v, lane,
+          [&](int rr) -> uint8_t* {
+            const int m = mw + rr;
+            return m < s.M ? reinterpret_cast<uint8_t*>(reinterpret_cast<T*>(p.out) +
+                                                        (int64_t)m * p.ld + nc)
+                           : nullptr;
+          },
+          [&](int q) { return nc + q * 8 + 8 <= s.N; });
     }
   }
 };
@@ -146,11 +179,12 @@ struct EpiSwiGLU {
   };
   template <int BN, bool BF16>
   static __device__ __forceinline__ void run(const Params& p, const TcShape& s, uint32_t tacc,
-                                             int m0, int nt, int row, int half) {
+                                             int m0, int nt, int row, int half, uint8_t* buf) {
     using P = Pack<BF16>;
     using T = typename P::T;
     constexpr int HALF = BN / 2;
-    const int m = m0 + row;
+    const int lane = row & 31;
+    const int mw = m0 + (row & ~31);
     const int j0 = nt * HALF;
     const bool keep_gu = p.g != nullptr;
 #pragma unroll 1
@@ -159,32 +193,28 @@ struct EpiSwiGLU {
       tmem_ld_32x32b_x32(tacc + c * 32, rg);
       tmem_ld_32x32b_x32(tacc + HALF + c * 32, ru);
       tmem_ld_wait();
-      if (m < s.M) {
+      uint32_t va[16], vg[16], vu[16];
 #pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) {
-          const int j = j0 + c * 32 + g8 * 8;
-          if (j + 8 <= s.N) {
-            uint4 va, vg, vu;
-            uint32_t* pa = &va.x;
-            uint32_t* pg = &vg.x;
-            uint32_t* pu = &vu.x;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float g0 = __uint_as_float(rg[g8 * 8 + 2 * e]);
-              const float g1 = __uint_as_float(rg[g8 * 8 + 2 * e + 1]);
-              const float u0 = __uint_as_float(ru[g8 * 8 + 2 * e]);
-              const float u1 = __uint_as_float(ru[g8 * 8 + 2 * e + 1]);
-              pa[e] = P::two(silu_f32(g0) * u0, silu_f32(g1) * u1);
-              pg[e] = P::two(g0, g1);
-              pu[e] = P::two(u0, u1);
-            }
-            *reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.a) + (int64_t)m * p.ld_a + j) = va;
-            if (keep_gu) {
-              *reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.g) + (int64_t)m * p.ld_gu + j) = vg;
-              *reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.u) + (int64_t)m * p.ld_gu + j) = vu;
-            }
-          }
-        }
+      for (int i = 0; i < 16; ++i) {
+        const float g0 = __uint_as_float(rg[2 * i]), g1 = __uint_as_float(rg[2 * i + 1]);
+        const float u0 = __uint_as_float(ru[2 * i]), u1 = __uint_as_float(ru[2 * i + 1]);
+        va[i] = P::two(silu_f32(g0) * u0, silu_f32(g1) * u1);
+        vg[i] = P::two(g0, g1);
+        vu[i] = P::two(u0, u1);
+      }
+      const int jc = j0 + c * 32;
+      auto ok = [&](int q) { return jc + q * 8 + 8 <= s.N; };
+      auto dst = [&](void* base, int64_t ld) {
+        return [=](int rr) -> uint8_t* {
+          const int m = mw + rr;
+          return m < s.M ? reinterpret_cast<uint8_t*>(reinterpret_cast<T*>(base) + (int64_t)m * ld + jc)
+                         : nullptr;
+        };
+      };
+      warp_store_tile(buf, va, lane, dst(p.a, p.ld_a), ok);
+      if (keep_gu) {
+        warp_store_tile(buf, vg, lane, dst(p.g, p.ld_gu), ok);
+        warp_store_tile(buf, vu, lane, dst(p.u, p.ld_gu), ok);
       }
     }
   }
@@ -222,15 +252,15 @@ struct EpiDSwiGLU {
   }
   template <int BN, bool BF16>
   static __device__ __forceinline__ void run(const Params& p, const TcShape& s, uint32_t tacc,
-                                             int m0, int nt, int row, int half) {
+                                             int m0, int nt, int row, int half, uint8_t* buf) {
     using P = Pack<BF16>;
     using T = typename P::T;
     const int m = m0 + row;
+    const int lane = row & 31;
+    const int mw = m0 + (row & ~31);
     const int jt = nt * BN;
     constexpr int CH = BN / 64;  // chunks of 32 columns per half
     const int c0 = half * CH;
-    T* grow = reinterpret_cast<T*>(p.g) + (int64_t)m * p.ld;
-    T* urow = reinterpret_cast<T*>(p.u) + (int64_t)m * p.ld;
     uint4 ng[4], nu[4];
     load_gu<BF16>(p, s, m, jt + c0 * 32, ng, nu);
 #pragma unroll 1
@@ -245,34 +275,43 @@ struct EpiDSwiGLU {
       uint32_t r[32];
       tmem_ld_32x32b_x32(tacc + c * 32, r);
       tmem_ld_wait();
-      if (m < s.M) {
+      uint32_t odg[16], odu[16];
 #pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) {
-          const int j = jt + c * 32 + g8 * 8;
-          if (j + 8 <= s.N) {
-            const uint32_t* pg = &vg[g8].x;
-            const uint32_t* pu = &vu[g8].x;
-            uint4 og, ou;
-            uint32_t* qg = &og.x;
-            uint32_t* qu = &ou.x;
+      for (int g8 = 0; g8 < 4; ++g8) {
+        const uint32_t* pg = &vg[g8].x;
+        const uint32_t* pu = &vu[g8].x;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 g = P::unpack(pg[e]);
-              const float2 u = P::unpack(pu[e]);
-              const float da0 = __uint_as_float(r[g8 * 8 + 2 * e]);
-              const float da1 = __uint_as_float(r[g8 * 8 + 2 * e + 1]);
-              const float s0 = 1.0f / (1.0f + __expf(-g.x));
-              const float s1 = 1.0f / (1.0f + __expf(-g.y));
-              const float ds0 = s0 * (1.0f + g.x * (1.0f - s0));
-              const float ds1 = s1 * (1.0f + g.y * (1.0f - s1));
-              qu[e] = P::two(da0 * (g.x * s0), da1 * (g.y * s1));
-              qg[e] = P::two(da0 * u.x * ds0, da1 * u.y * ds1);
-            }
-            *reinterpret_cast<uint4*>(grow + j) = og;
-            *reinterpret_cast<uint4*>(urow + j) = ou;
-          }
+        for (int e = 0; e < 4; ++e) {
+          const float2 g = P::unpack(pg[e]);
+          const float2 u = P::unpack(pu[e]);
+          const float da0 = __uint_as_float(r[g8 * 8 + 2 * e]);
+          const float da1 = __uint_as_float(r[g8 * 8 + 2 * e + 1]);
+          const float s0 = 1.0f / (1.0f + __expf(-g.x));
+          const float s1 = 1.0f / (1.0f + __expf(-g.y));
+          const float ds0 = s0 * (1.0f + g.x * (1.0f - s0));
+          const float ds1 = s1 * (1.0f + g.y * (1.0f - s1));
+          odu[g8 * 4 + e] = P::two(da0 * (g.x * s0), da1 * (g.y * s1));
+          odg[g8 * 4 + e] = P::two(da0 * u.x * ds0, da1 * u.y * ds1);
         }
       }
+      const int jc = jt + c * 32;
+      auto ok = [&](int q) { return jc + q * 8 + 8 <= s.N; };
+      warp_store_tile(buf, odg, lane,
+                      [&](int rr) -> uint8_t* {
+                        const int mm = mw + rr;
+                        return mm < s.M ? reinterpret_cast<uint8_t*>(reinterpret_cast<T*>(p.g) +
+                                                                     (int64_t)mm * p.ld + jc)
+                                        : nullptr;
+                      },
+                      ok);
+      warp_store_tile(buf, odu, lane,
+                      [&](int rr) -> uint8_t* {
+                        const int mm = mw + rr;
+                        return mm < s.M ? reinterpret_cast<uint8_t*>(reinterpret_cast<T*>(p.u) +
+                                                                     (int64_t)mm * p.ld + jc)
+                                        : nullptr;
+                      },
+                      ok);
     }
   }
 };
@@ -285,9 +324,11 @@ struct TcSmem {
   static constexpr int A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
   static constexpr int B_BYTES = BN * TC_BK * 2;     // 32 KB for BN = 256
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES + 8 * 2048;
   // barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
   static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;         // 8 warps x 2 KB store staging
+  static constexpr int EPI_BYTES = 8 * 2048;
   static constexpr int MISC_OFFSET = BAR_OFFSET + NUM_BARS * 8;  // tmem slot, abort flag
   static constexpr int TOTAL = MISC_OFFSET + 16;
   static constexpr int DYN_BYTES = TOTAL + 1024;  // slack for 1024-byte alignment
@@ -477,7 +518,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int mt, nt;
       tc_tile_coords(t, s, mt, nt);
       const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      Epi::template run<BN, BF16>(ep, s, tacc, mt * TC_BM, nt, row, half);
+      Epi::template run<BN, BF16>(ep, s, tacc, mt * TC_BM, nt, row, half,
+                                  smem + L::EPI_OFFSET + (warp - 2) * 2048);
       tc_fence_before();
       mbar_arrive(acce_bar(acc));
       if (++acc == 2) {
