@@ -174,12 +174,18 @@ TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err
   s.wait_limit_ns = g_wait_limit_ns.load();
   s.err = err;
   s.inject_stall = g_inject_stall.exchange(0);
+  s.pdl_wait_start = 0;
+  s.pdl_wait_end = 0;
   return s;
 }
 
+// pdl: launch as a programmatic dependent of the previous kernel on the
+// stream (s.pdl_wait_start / s.pdl_wait_end say what it must wait for).
+// Per-kernel event timing puts events between the kernels, so it launches
+// them in plain stream order instead.
 template <int AM, int BMODE, bool BF16, class Epi>
 cudaError_t launch_tc(int kid, const CUtensorMap& ta, const CUtensorMap& tb, const TcShape& s,
-                      const typename Epi::Params& ep, cudaStream_t st) {
+                      const typename Epi::Params& ep, cudaStream_t st, bool pdl = false) {
   auto kern = tc_gemm_kernel<TC_BN, TC_STAGES, AM, BMODE, BF16, Epi>;
   constexpr int smem = TcSmem<TC_BN, TC_STAGES>::DYN_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -188,8 +194,20 @@ cudaError_t launch_tc(int kid, const CUtensorMap& ta, const CUtensorMap& tb, con
   const int nsm = sm_count();
   const int grid = tiles < nsm ? tiles : nsm;
   ProfScope prof(kid, st);
-  kern<<<grid, TC_THREADS, smem, st>>>(ta, tb, s, ep);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  const bool use_pdl = pdl && !g_prof_on.load();
+  cfg.attrs = use_pdl ? attr : nullptr;
+  cfg.numAttrs = use_pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, s, ep);
   g_last_launches.fetch_add(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -415,9 +433,10 @@ swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y
   if (!map_kmajor(&ta, BF16, A, H, M, ld_a, TC_BM) || !map_kmajor(&twd, BF16, Wd, H, D, H, TC_BN))
     return SWIGLU_ERR_CUDA;
   TcShape s2 = make_shape(M, D, H, TC_BN, err);
+  s2.pdl_wait_start = 1;  // reads A
   EpiStore::Params p2{Y, D};
   return cuda_status(launch_tc<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore>(
-      G != nullptr ? K_DOWN : K_DOWN_NOGRAD, ta, twd, s2, p2, st));
+      G != nullptr ? K_DOWN : K_DOWN_NOGRAD, ta, twd, s2, p2, st, true));
 }
 
 template <bool BF16>
@@ -431,15 +450,11 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   void* A = sv + 2 * H * 2;
   CUtensorMap m1, m2;
   cudaError_t e;
-  // dA = dY Wd (Wd read MN-major as [K = D][N = H]); dG, dU in place
-  if (!map_kmajor(&m1, BF16, dY, D, M, D, TC_BM) || !map_mnmajor(&m2, BF16, Wd, H, D, H))
-    return SWIGLU_ERR_CUDA;
-  {
-    TcShape s = make_shape(M, H, D, TC_BN, err);
-    EpiDSwiGLU::Params p{G, U, ld};
-    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLU>(K_DGU, m1, m2, s, p, st);
-    if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
-  }
+  // Order: dWd, then dG/dU as its programmatic dependent (independent of
+  // dWd: it fills dWd's last partial wave, and waits for dWd at its end);
+  // dWgu after dG/dU (waits for it at the start); dX as dWgu's dependent
+  // (needs only dG/dU, fills dWgu's last wave, waits for dWgu at its end).
+  //
   // dWd [D, H] = dY^T A: both operands MN-major over the token dimension
   if (!map_mnmajor(&m1, BF16, dY, D, M, D) || !map_mnmajor(&m2, BF16, A, H, M, ld))
     return SWIGLU_ERR_CUDA;
@@ -449,13 +464,24 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     e = launch_tc<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DWD, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
+  // dA = dY Wd (Wd read MN-major as [K = D][N = H]); dG, dU written over G, U
+  if (!map_kmajor(&m1, BF16, dY, D, M, D, TC_BM) || !map_mnmajor(&m2, BF16, Wd, H, D, H))
+    return SWIGLU_ERR_CUDA;
+  {
+    TcShape s = make_shape(M, H, D, TC_BN, err);
+    s.pdl_wait_end = 1;
+    EpiDSwiGLU::Params p{G, U, ld};
+    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLU>(K_DGU, m1, m2, s, p, st, true);
+    if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
+  }
   // [dWg; dWu] [2H, D] = [dG | dU]^T X: one GEMM over the 2H columns
   if (!map_mnmajor(&m1, BF16, G, 2 * H, M, ld) || !map_mnmajor(&m2, BF16, X, D, M, D))
     return SWIGLU_ERR_CUDA;
   {
     TcShape s = make_shape(2 * H, D, M, TC_BN, err);
+    s.pdl_wait_start = 1;  // reads dG, dU
     EpiStore::Params p{dWgu, D};
-    e = launch_tc<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DWGU, m1, m2, s, p, st);
+    e = launch_tc<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DWGU, m1, m2, s, p, st, true);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   // dX [M, D] = [dG | dU] [Wg; Wu]: K = 2H in one accumulator
@@ -463,8 +489,9 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     return SWIGLU_ERR_CUDA;
   {
     TcShape s = make_shape(M, D, 2 * H, TC_BN, err);
+    s.pdl_wait_end = 1;
     EpiStore::Params p{dX, D};
-    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DX, m1, m2, s, p, st);
+    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DX, m1, m2, s, p, st, true);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   return SWIGLU_OK;

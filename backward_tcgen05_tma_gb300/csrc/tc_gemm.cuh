@@ -46,6 +46,13 @@ struct TcShape {
   uint64_t wait_limit_ns;
   int* err;              // device error word (workspace)
   int inject_stall;      // test hook: producer skips stage 0 of its first tile
+  // Programmatic dependent launch (the kernel may start while the previous
+  // kernel on the stream is still running): wait for the previous kernel at
+  // the start (it reads what that kernel writes) and/or at the end (so the
+  // kernel does not complete before it, keeping the stream's order for
+  // whatever follows).  Both are no-ops in an ordinary launch.
+  int pdl_wait_start;
+  int pdl_wait_end;
 };
 
 // Tile order: groups of group_m m-tiles, m fastest inside a group, so the CTAs
@@ -363,6 +370,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // the next kernel may be scheduled once every CTA is past this point; a
+  // kernel that depends on its predecessor's output signals only after
+  // waiting for it, so its own dependents never start before that output exists
+  if (s.pdl_wait_start) pdl_wait();
+  pdl_launch_dependents();
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(full_bar(i), 1);
@@ -536,6 +549,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, L::TMEM_COLS);
   }
+  if (s.pdl_wait_end && threadIdx.x == 0) pdl_wait();
 }
 
 }  // namespace swiglu
