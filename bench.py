@@ -139,6 +139,19 @@ def _dist():
     return world, rank, local
 
 
+def aggregate_over_ranks(sec: float, flops_per_rank: float, world: int, device="cpu"):
+    """Replicas: every rank times its own steps; the job's step time is the
+    slowest rank's (all_reduce MAX) and the job's throughput counts every
+    rank's work.  Returns (max seconds per step, job TFLOPS)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([sec], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        sec = float(t.item())
+    return sec, flops_per_rank * world / sec / 1e12
+
+
 def _config(workload, w, dtype, world):
     return {"workload": workload, "B": w["B"], "S": w["S"], "D": w["D"], "H": w["H"],
             "M": w["B"] * w["S"], "dtype": dtype, "parallelism": "replicas%d" % world,
@@ -386,13 +399,10 @@ def run_ours(args):
     sec, launches, prof, (t, o) = _time_training(api, w, "bf16", args.steps, args.warmup,
                                                  seed=rank, device=device, profile=True)
     clocks = sampler.stop()
-    if world > 1:
-        mx = torch.tensor([sec], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
-        sec = float(mx.item())
-        torch.distributed.barrier()
     flops = metrics.fwd_bwd_flops(M, D, H)
-    value = flops * world / sec / 1e12
+    sec, value = aggregate_over_ranks(sec, flops, world, device)
+    if world > 1:
+        torch.distributed.barrier()
 
     # dominant kernel from live event timings of the timed region
     dom = max(prof.items(), key=lambda kv: kv[1][1])
