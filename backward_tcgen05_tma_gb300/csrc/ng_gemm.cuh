@@ -17,6 +17,11 @@
 //            rows of the same units (one 3-D TMA box), so the partial sums of
 //            G and U meet in one CTA: A = rnd(SiLU(g) * u) -> A [M, H];
 //   down:    tile = 128 output features of Wd; Y = rnd(sum) -> Y [M, D].
+// When there are at least as many tiles as CTAs the split is a hybrid: the
+// first tiles (tiles mod CTAs of them) are shared stream-K style and every CTA
+// streams its share of those first, so their reductions happen mid-kernel;
+// then each CTA takes whole tiles, whose epilogue writes the output straight
+// from TMEM (no partial, no counter, no reduction at the end of the kernel).
 // No CTA ever waits for another CTA: a segment that is not last moves on.
 // The down kernel is launched as a programmatic dependent of the gate/up
 // kernel: its CTAs start streaming Wd into the ring while gate/up drains, and
@@ -32,7 +37,9 @@ struct NgArgs {
   int rows;         // gate/up: H (hidden units); down: D (output features)
   int kb_tile;      // k-blocks of 64 in one tile's contraction
   int tiles;
-  int seg_max;      // partial slots per CTA (>= segments of any CTA's range)
+  int sk_tiles;     // tiles [0, sk_tiles) are shared stream-K; the rest are whole,
+                    //   (tiles - sk_tiles) / gridDim.x per CTA
+  int seg_max;      // partial slots per CTA (>= stream-K segments of any CTA)
   float* part;      // [gridDim.x * seg_max][128][NT] fp32 partial tiles
   int* counters;    // [tiles] arrival counters, zero at launch
   int* zero_ptr;    // block 0 zeroes zero_ptr[0 .. zero_count): the other
@@ -50,8 +57,10 @@ struct NgSmem {
   static constexpr int W_BYTES = 128 * 64 * 2;  // 16 KB of weights per k-block
   static constexpr int X_BYTES = NT * 64 * 2;   // the tokens' k-block
   static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
-  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;  // ~200 KB of weights in flight
-  static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+  static constexpr int USTAGE_BYTES = 64 * NT * 4;  // U rows of a whole gate/up tile
+  static constexpr int STAGES = (200 * 1024 - USTAGE_BYTES) / STAGE_BYTES;
+  static constexpr int USTAGE_OFFSET = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFFSET = USTAGE_OFFSET + USTAGE_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, acc_full[2], acc_empty[2], drain
   static constexpr int MISC_OFFSET = BAR_OFFSET + NUM_BARS * 8;
   static constexpr int TOTAL = MISC_OFFSET + 16;
@@ -66,6 +75,33 @@ __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;"
 __device__ __forceinline__ int64_t ng_start(int64_t c, int64_t total, int64_t ctas) {
   return c * total / ctas;
 }
+
+// This CTA's sequence of segments: its stream-K range first, then its whole
+// tiles.
+struct NgSegIter {
+  int64_t x, x_end;   // stream-K k-block range still to cover
+  int dp, dp_count;   // whole tiles taken / to take
+  int kb_tile, sk_tiles, cta, ctas;
+  __device__ __forceinline__ bool next(int& tile, int& kb0, int& nkb, bool& whole) {
+    if (x < x_end) {
+      tile = (int)(x / kb_tile);
+      kb0 = (int)(x - (int64_t)tile * kb_tile);
+      nkb = (int)min((int64_t)(kb_tile - kb0), x_end - x);
+      x += nkb;
+      whole = false;
+      return true;
+    }
+    if (dp < dp_count) {
+      tile = sk_tiles + cta + dp * ctas;
+      kb0 = 0;
+      nkb = kb_tile;
+      ++dp;
+      whole = true;
+      return true;
+    }
+    return false;
+  }
+};
 
 // The CTA whose range holds global k-block x.
 __device__ __forceinline__ int ng_owner(int64_t x, int64_t total, int64_t ctas) {
@@ -100,7 +136,9 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
   static_assert(NT == 16 || NT == 32 || NT == 64, "NT must be 16, 32 or 64");
   static_assert(L::TOTAL + 1024 <= 232448, "shared memory plan exceeds 227 KB");
   constexpr int TILE_ROWS = GATE_UP ? 64 : 128;  // output rows (hidden units / features) per tile
-  constexpr int RB = NT <= 16 ? 4 : (NT <= 32 ? 2 : 1);  // partials loaded per reduction batch
+  // partials loaded per reduction batch (the down kernel's tiles have more
+  // contributors; its per-thread partial is half the gate/up one's pair)
+  constexpr int RB = GATE_UP ? (NT <= 16 ? 4 : (NT <= 32 ? 2 : 1)) : (NT <= 16 ? 8 : (NT <= 32 ? 4 : 2));
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -152,10 +190,15 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int64_t total = (int64_t)a.tiles * a.kb_tile;  // k-blocks of the whole launch
+  const int64_t total = (int64_t)a.sk_tiles * a.kb_tile;  // stream-K k-blocks
   const int64_t ctas = gridDim.x;
   const int64_t x_begin = ng_start(blockIdx.x, total, ctas);
   const int64_t x_end = ng_start(blockIdx.x + 1, total, ctas);
+  const int dp_count = (a.tiles - a.sk_tiles) / gridDim.x;
+  auto segs = [&]() {
+    return NgSegIter{x_begin, x_end, 0, dp_count, a.kb_tile, a.sk_tiles, (int)blockIdx.x,
+                     (int)gridDim.x};
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -169,20 +212,22 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
       int pending_x = 0;  // ring slots holding weights whose activation load is deferred
       int32_t pending_k0[L::STAGES];
       if (a.dependent) {
-        int64_t x = x_begin;
-        while (x < x_end && pending_x < L::STAGES) {
-          const int tile = (int)(x / a.kb_tile);
-          const int k0 = (int)(x - (int64_t)tile * a.kb_tile) * TC_BK;
-          const uint32_t sw = sbase + pending_x * L::STAGE_BYTES;
-          mbar_arrive_expect_tx(full_bar(pending_x), L::STAGE_BYTES);
-          if (GATE_UP)
-            tma_load_3d(sw, &tmW, full_bar(pending_x), k0, tile * TILE_ROWS, 0);
-          else
-            tma_load_2d(sw, &tmW, full_bar(pending_x), k0, tile * TILE_ROWS);
-          pending_k0[pending_x] = k0;
-          issued_mask |= 1u << pending_x;
-          ++pending_x;
-          ++x;
+        NgSegIter it = segs();
+        int tile, kb0, nkb;
+        bool whole;
+        while (pending_x < L::STAGES && it.next(tile, kb0, nkb, whole)) {
+          for (int i = 0; i < nkb && pending_x < L::STAGES; ++i) {
+            const int k0 = (kb0 + i) * TC_BK;
+            const uint32_t sw = sbase + pending_x * L::STAGE_BYTES;
+            mbar_arrive_expect_tx(full_bar(pending_x), L::STAGE_BYTES);
+            if (GATE_UP)
+              tma_load_3d(sw, &tmW, full_bar(pending_x), k0, tile * TILE_ROWS, 0);
+            else
+              tma_load_2d(sw, &tmW, full_bar(pending_x), k0, tile * TILE_ROWS);
+            pending_k0[pending_x] = k0;
+            issued_mask |= 1u << pending_x;
+            ++pending_x;
+          }
         }
         pdl_wait();
         if (blockIdx.x == 0)
@@ -191,11 +236,10 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
           tma_load_2d(sbase + i * L::STAGE_BYTES + L::W_BYTES, &tmX, full_bar(i), pending_k0[i], 0);
       }
       int skip = pending_x;  // k-blocks already issued above
-      for (int64_t x = x_begin; x < x_end && ok;) {
-        const int tile = (int)(x / a.kb_tile);
-        const int kb0 = (int)(x - (int64_t)tile * a.kb_tile);
-        const int nkb = (int)min((int64_t)(a.kb_tile - kb0), x_end - x);
-        x += nkb;
+      NgSegIter it = segs();
+      int tile, kb0, nkb;
+      bool whole;
+      while (ok && it.next(tile, kb0, nkb, whole)) {
         for (int i = 0; i < nkb; ++i) {
           if (skip > 0) {
             --skip;
@@ -242,11 +286,10 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int64_t x = x_begin; x < x_end && ok;) {
-        const int tile = (int)(x / a.kb_tile);
-        const int kb0 = (int)(x - (int64_t)tile * a.kb_tile);
-        const int nkb = (int)min((int64_t)(a.kb_tile - kb0), x_end - x);
-        x += nkb;
+      NgSegIter it = segs();
+      int tile, kb0, nkb;
+      bool whole;
+      while (ok && it.next(tile, kb0, nkb, whole)) {
         if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, a.wait_limit_ns, abort_flag, a.err)) {
           ok = false;
           break;
@@ -289,15 +332,77 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int seg = 0;
-    for (int64_t x = x_begin; x < x_end; ++seg) {
-      const int tile = (int)(x / a.kb_tile);
-      const int kb0 = (int)(x - (int64_t)tile * a.kb_tile);
-      x += min((int64_t)(a.kb_tile - kb0), x_end - x);
+    NgSegIter it = segs();
+    int tile, kb0, nkb;
+    bool whole;
+    float* ustage = reinterpret_cast<float*>(smem + L::USTAGE_OFFSET);
+    for (; it.next(tile, kb0, nkb, whole); ++seg) {
       int ok = 1;
       if (lane == 0)
         ok = mbar_wait_bounded(accf_bar(acc), acc_phase, a.wait_limit_ns, abort_flag, a.err) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!epi_bar_and(ok)) break;  // all four epilogue warps leave together
+      if (whole) {
+        // whole tile: the output straight from TMEM
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * NT;
+        float v[NT];
+#pragma unroll
+        for (int c = 0; c < NT; c += 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(taddr + c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 16; ++q) v[c + q] = __uint_as_float(r[q]);
+        }
+        tc_fence_before();
+        mbar_arrive(acce_bar(acc));
+        if (GATE_UP) {
+          // rows 64..127 (U) hand their values to rows 0..63 (G) of the same unit
+          if (row >= 64) {
+#pragma unroll
+            for (int n = 0; n < NT; n += 4)
+              *reinterpret_cast<float4*>(ustage + (row - 64) * NT + n) =
+                  make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
+          }
+          epi_bar_sync();
+          const int j = tile * 64 + row;
+          if (row < 64 && j < a.rows) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              if (n < a.M) {
+                const float o = silu_f32(v[n]) * ustage[row * NT + n];
+                if (BF16)
+                  reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)n * a.ld_out + j] =
+                      __float2bfloat16_rn(o);
+                else
+                  reinterpret_cast<__half*>(a.out)[(int64_t)n * a.ld_out + j] = __float2half_rn(o);
+              }
+            }
+          }
+          epi_bar_sync();  // ustage is free again
+        } else {
+          const int d = tile * 128 + row;
+          if (d < a.rows) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              if (n < a.M) {
+                if (BF16)
+                  reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)n * a.ld_out + d] =
+                      __float2bfloat16_rn(v[n]);
+                else
+                  reinterpret_cast<__half*>(a.out)[(int64_t)n * a.ld_out + d] =
+                      __float2half_rn(v[n]);
+              }
+            }
+          }
+        }
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+        continue;
+      }
       {
         tc_fence_after();
         float* dst = a.part + (((size_t)blockIdx.x * a.seg_max + seg) * 128 + row) * NT;

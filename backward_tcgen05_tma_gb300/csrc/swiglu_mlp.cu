@@ -174,18 +174,16 @@ TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err
   s.wait_limit_ns = g_wait_limit_ns.load();
   s.err = err;
   s.inject_stall = g_inject_stall.exchange(0);
-  s.pdl_wait_start = 0;
-  s.pdl_wait_end = 0;
   return s;
 }
 
-// pdl: launch as a programmatic dependent of the previous kernel on the
-// stream (s.pdl_wait_start / s.pdl_wait_end say what it must wait for).
-// Per-kernel event timing puts events between the kernels, so it launches
-// them in plain stream order instead.
+// The training kernels are launched in plain stream order: with a static
+// round-robin tile split, a programmatic dependent whose CTAs start late on
+// SMs still held by the predecessor's last wave also finishes late (measured
+// slower than plain order).
 template <int AM, int BMODE, bool BF16, class Epi>
 cudaError_t launch_tc(int kid, const CUtensorMap& ta, const CUtensorMap& tb, const TcShape& s,
-                      const typename Epi::Params& ep, cudaStream_t st, bool pdl = false) {
+                      const typename Epi::Params& ep, cudaStream_t st) {
   auto kern = tc_gemm_kernel<TC_BN, TC_STAGES, AM, BMODE, BF16, Epi>;
   constexpr int smem = TcSmem<TC_BN, TC_STAGES>::DYN_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -194,20 +192,8 @@ cudaError_t launch_tc(int kid, const CUtensorMap& ta, const CUtensorMap& tb, con
   const int nsm = sm_count();
   const int grid = tiles < nsm ? tiles : nsm;
   ProfScope prof(kid, st);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(TC_THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  const bool use_pdl = pdl && !g_prof_on.load();
-  cfg.attrs = use_pdl ? attr : nullptr;
-  cfg.numAttrs = use_pdl ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, s, ep);
+  kern<<<grid, TC_THREADS, smem, st>>>(ta, tb, s, ep);
   g_last_launches.fetch_add(1);
-  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -255,14 +241,17 @@ NgPlan ng_plan(int64_t M, int64_t D, int64_t H) {
   return p;
 }
 
-void ng_grid(int tiles, int kb, int& ctas, int& seg_max) {
-  const int64_t total = (int64_t)tiles * kb;
+// Grid, stream-K tiles and partial slots per CTA.  With tiles >= CTAs, all
+// but (tiles mod CTAs) tiles are taken whole, the same number per CTA.
+void ng_grid(int tiles, int kb, int& ctas, int& sk_tiles, int& seg_max) {
   int nsm = sm_count();
   if (nsm < 1) nsm = 1;
   int64_t c = nsm < NG_MAX_CTAS ? nsm : NG_MAX_CTAS;
-  if (c > total) c = total;
+  sk_tiles = tiles >= c ? (int)(tiles % c) : tiles;
+  const int64_t total = (int64_t)sk_tiles * kb;
+  if (total > 0 && c > total && tiles < c) c = total;
   ctas = (int)c;
-  const int64_t range = (total + c - 1) / c;
+  const int64_t range = total > 0 ? (total + c - 1) / c : 0;
   seg_max = (int)((range + kb - 1) / kb) + 1;
 }
 
@@ -274,7 +263,7 @@ cudaError_t launch_ng(int kid, const CUtensorMap& tw, const CUtensorMap& tx, NgA
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int grid = 1;
-  ng_grid(a.tiles, a.kb_tile, grid, a.seg_max);
+  ng_grid(a.tiles, a.kb_tile, grid, a.sk_tiles, a.seg_max);
   ProfScope prof(kid, st);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -312,13 +301,13 @@ swiglu_status ng_forward_nt(const void* X, const void* Wgu, const void* Wd, void
   CUtensorMap tw, tx;
   if (!encode_gateup(&tw, BF16, Wgu, D, H, 64) || !map_kmajor(&tx, BF16, X, D, M, D, NT))
     return SWIGLU_ERR_CUDA;
-  NgArgs a1{(int)M, (int)H, p.kb1, p.t1, 0, part, counters, counters + p.t1, p.t2, 1, 0,
+  NgArgs a1{(int)M, (int)H, p.kb1, p.t1, 0, 0, part, counters, counters + p.t1, p.t2, 1, 0,
             A, H, wl, err};
   if (launch_ng<NT, true, BF16>(K_NG_GATE_UP, tw, tx, a1, st) != cudaSuccess)
     return SWIGLU_ERR_CUDA;
   if (!map_kmajor(&tw, BF16, Wd, H, D, H, 128) || !map_kmajor(&tx, BF16, A, H, M, H, NT))
     return SWIGLU_ERR_CUDA;
-  NgArgs a2{(int)M, (int)D, p.kb2, p.t2, 0, part, counters + p.t1, counters, p.t1, 0, 1,
+  NgArgs a2{(int)M, (int)D, p.kb2, p.t2, 0, 0, part, counters + p.t1, counters, p.t1, 0, 1,
             Y, D, wl, err};
   return cuda_status(launch_ng<NT, false, BF16>(K_NG_DOWN, tw, tx, a2, st));
 }
@@ -367,9 +356,9 @@ swiglu_status noalloc_scratch(void** out) {
 
 // Scratch bytes one call needs on the current device (its actual grids).
 size_t noalloc_bytes_needed(const NgPlan& p) {
-  int c1 = 1, s1 = 1, c2 = 1, s2 = 1;
-  ng_grid(p.t1, p.kb1, c1, s1);
-  ng_grid(p.t2, p.kb2, c2, s2);
+  int c1 = 1, s1 = 1, c2 = 1, s2 = 1, k1 = 0, k2 = 0;
+  ng_grid(p.t1, p.kb1, c1, k1, s1);
+  ng_grid(p.t2, p.kb2, c2, k2, s2);
   const size_t slots1 = (size_t)c1 * s1, slots2 = (size_t)c2 * s2;
   return WS_HEADER + p.counter_bytes + (slots1 > slots2 ? slots1 : slots2) * 128 * p.NT * 4;
 }
@@ -433,10 +422,9 @@ swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y
   if (!map_kmajor(&ta, BF16, A, H, M, ld_a, TC_BM) || !map_kmajor(&twd, BF16, Wd, H, D, H, TC_BN))
     return SWIGLU_ERR_CUDA;
   TcShape s2 = make_shape(M, D, H, TC_BN, err);
-  s2.pdl_wait_start = 1;  // reads A
   EpiStore::Params p2{Y, D};
   return cuda_status(launch_tc<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore>(
-      G != nullptr ? K_DOWN : K_DOWN_NOGRAD, ta, twd, s2, p2, st, true));
+      G != nullptr ? K_DOWN : K_DOWN_NOGRAD, ta, twd, s2, p2, st));
 }
 
 template <bool BF16>
@@ -450,11 +438,6 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   void* A = sv + 2 * H * 2;
   CUtensorMap m1, m2;
   cudaError_t e;
-  // Order: dWd, then dG/dU as its programmatic dependent (independent of
-  // dWd: it fills dWd's last partial wave, and waits for dWd at its end);
-  // dWgu after dG/dU (waits for it at the start); dX as dWgu's dependent
-  // (needs only dG/dU, fills dWgu's last wave, waits for dWgu at its end).
-  //
   // dWd [D, H] = dY^T A: both operands MN-major over the token dimension
   if (!map_mnmajor(&m1, BF16, dY, D, M, D) || !map_mnmajor(&m2, BF16, A, H, M, ld))
     return SWIGLU_ERR_CUDA;
@@ -469,9 +452,8 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     return SWIGLU_ERR_CUDA;
   {
     TcShape s = make_shape(M, H, D, TC_BN, err);
-    s.pdl_wait_end = 1;
     EpiDSwiGLU::Params p{G, U, ld};
-    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLU>(K_DGU, m1, m2, s, p, st, true);
+    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLU>(K_DGU, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   // [dWg; dWu] [2H, D] = [dG | dU]^T X: one GEMM over the 2H columns
@@ -479,9 +461,8 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     return SWIGLU_ERR_CUDA;
   {
     TcShape s = make_shape(2 * H, D, M, TC_BN, err);
-    s.pdl_wait_start = 1;  // reads dG, dU
     EpiStore::Params p{dWgu, D};
-    e = launch_tc<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DWGU, m1, m2, s, p, st, true);
+    e = launch_tc<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DWGU, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   // dX [M, D] = [dG | dU] [Wg; Wu]: K = 2H in one accumulator
@@ -489,9 +470,8 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     return SWIGLU_ERR_CUDA;
   {
     TcShape s = make_shape(M, D, 2 * H, TC_BN, err);
-    s.pdl_wait_end = 1;
     EpiStore::Params p{dX, D};
-    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DX, m1, m2, s, p, st, true);
+    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DX, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   return SWIGLU_OK;

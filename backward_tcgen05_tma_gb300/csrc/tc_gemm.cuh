@@ -46,13 +46,6 @@ struct TcShape {
   uint64_t wait_limit_ns;
   int* err;              // device error word (workspace)
   int inject_stall;      // test hook: producer skips stage 0 of its first tile
-  // Programmatic dependent launch (the kernel may start while the previous
-  // kernel on the stream is still running): wait for the previous kernel at
-  // the start (it reads what that kernel writes) and/or at the end (so the
-  // kernel does not complete before it, keeping the stream's order for
-  // whatever follows).  Both are no-ops in an ordinary launch.
-  int pdl_wait_start;
-  int pdl_wait_end;
 };
 
 // Tile order: groups of group_m m-tiles, m fastest inside a group, so the CTAs
@@ -133,8 +126,10 @@ __device__ __forceinline__ void warp_store_tile(uint8_t* buf, const uint32_t (&v
   __syncwarp();
 }
 
-// SiLU(g) = g / (1 + e^-g), evaluated in fp32.
-__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + __expf(-g)); }
+// sigma(g) = 1 / (1 + e^-g) in fp32 with a correctly rounded reciprocal
+// (exact limits: e^-g = inf gives 0); SiLU(g) = g * sigma(g).
+__device__ __forceinline__ float sigmoid_f32(float g) { return __frcp_rn(1.0f + __expf(-g)); }
+__device__ __forceinline__ float silu_f32(float g) { return g * sigmoid_f32(g); }
 
 // Plain store: C[m, n] = rnd(acc).
 struct EpiStore {
@@ -293,8 +288,8 @@ struct EpiDSwiGLU {
           const float2 u = P::unpack(pu[e]);
           const float da0 = __uint_as_float(r[g8 * 8 + 2 * e]);
           const float da1 = __uint_as_float(r[g8 * 8 + 2 * e + 1]);
-          const float s0 = 1.0f / (1.0f + __expf(-g.x));
-          const float s1 = 1.0f / (1.0f + __expf(-g.y));
+          const float s0 = sigmoid_f32(g.x);
+          const float s1 = sigmoid_f32(g.y);
           const float ds0 = s0 * (1.0f + g.x * (1.0f - s0));
           const float ds1 = s1 * (1.0f + g.y * (1.0f - s1));
           odu[g8 * 4 + e] = P::two(da0 * (g.x * s0), da1 * (g.y * s1));
@@ -369,12 +364,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // the next kernel may be scheduled once every CTA is past this point; a
-  // kernel that depends on its predecessor's output signals only after
-  // waiting for it, so its own dependents never start before that output exists
-  if (s.pdl_wait_start) pdl_wait();
-  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -549,7 +538,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, L::TMEM_COLS);
   }
-  if (s.pdl_wait_end && threadIdx.x == 0) pdl_wait();
 }
 
 }  // namespace swiglu
