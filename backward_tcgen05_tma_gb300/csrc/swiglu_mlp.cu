@@ -162,6 +162,71 @@ bool map_mnmajor(CUtensorMap* tm, bool bf16, const void* base, int64_t MN, int64
   return encode_2d(tm, bf16, base, (uint64_t)MN, (uint64_t)K, (uint64_t)ld * 2, 64, 64);
 }
 
+// ---------------------------------------------------------------------------
+// stream-K hybrid for the tensor-core kernels
+// ---------------------------------------------------------------------------
+// Workspace of a training call: [0, 256) header (error word), then the
+// shared-tile counters, then the fp32 partial tiles.
+constexpr size_t TC_SK_COUNTER_BYTES = 1024;  // up to 256 shared tiles
+constexpr int TC_SK_MAX_SMS = 256;
+
+struct TcPlan {
+  int grid, sk_tiles, seg_max;
+};
+
+// Whole tiles round-robin, unless the last round would leave more than 3% of
+// the SMs' time idle: then the (tiles mod SMs) tiles of that round (all of
+// them when there are fewer tiles than SMs) are shared stream-K style.  A
+// CTA's shared range is at most one tile long, so it meets at most two tiles.
+TcPlan tc_plan(int64_t tiles, int64_t kb, int nsm) {
+  TcPlan p{(int)(tiles < nsm ? tiles : nsm), 0, 1};
+  const int64_t waves = (tiles + nsm - 1) / nsm;
+  const double fill = (double)tiles / ((double)waves * nsm);
+  if (fill >= 0.97 || kb < 8) return p;
+  p.sk_tiles = (int)(tiles >= nsm ? tiles % nsm : tiles);
+  const int64_t total = (int64_t)p.sk_tiles * kb;
+  p.grid = nsm;
+  if (tiles < nsm && total < nsm) p.grid = (int)total;
+  const int64_t range = (total + p.grid - 1) / p.grid;
+  p.seg_max = (int)((range + kb - 1) / kb) + 1;
+  return p;
+}
+
+// Bytes of the workspace that must be zero when a training call starts: the
+// error word, and the shared-tile counters of the tensor-core kernels.
+size_t ws_clear_bytes(swiglu_dtype dt) {
+  return dt == SWIGLU_F32_IEEE ? sizeof(int) : WS_HEADER + TC_SK_COUNTER_BYTES;
+}
+
+size_t tc_part_bytes(const TcPlan& p) {
+  return p.sk_tiles ? (size_t)p.grid * p.seg_max * TC_BM * TC_BN * 4 : 0;
+}
+
+int tc_nsm() {
+  const int n = sm_count();
+  return n < 1 ? 1 : (n > TC_SK_MAX_SMS ? TC_SK_MAX_SMS : n);
+}
+
+// Partial-tile bytes a training call needs: its tensor-core GEMMs as
+// (GEMM rows, GEMM columns, columns per tile, K).  Without a device the bound
+// for any GPU of up to 256 SMs (two slots per CTA).
+size_t tc_ws_part_bytes(int64_t M, int64_t D, int64_t H, int op) {
+  if (sm_count() < 1) return (size_t)2 * TC_SK_MAX_SMS * TC_BM * TC_BN * 4;
+  const int nsm = tc_nsm();
+  const int64_t fwd[2][4] = {{M, H, TC_BN / 2, D}, {M, D, TC_BN, H}};
+  const int64_t bwd[4][4] = {{D, H, TC_BN, M}, {M, H, TC_BN, D}, {2 * H, D, TC_BN, M},
+                             {M, D, TC_BN, 2 * H}};
+  size_t best = 0;
+  const int n = op == SWIGLU_OP_BWD ? 4 : 2;
+  for (int i = 0; i < n; ++i) {
+    const int64_t* g = op == SWIGLU_OP_BWD ? bwd[i] : fwd[i];
+    const int64_t tiles = ((g[0] + TC_BM - 1) / TC_BM) * ((g[1] + g[2] - 1) / g[2]);
+    const size_t b = tc_part_bytes(tc_plan(tiles, (g[3] + TC_BK - 1) / TC_BK, nsm));
+    if (b > best) best = b;
+  }
+  return best;
+}
+
 TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err) {
   TcShape s;
   s.M = (int)M;
@@ -174,6 +239,12 @@ TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err
   s.wait_limit_ns = g_wait_limit_ns.load();
   s.err = err;
   s.inject_stall = g_inject_stall.exchange(0);
+  // the workspace (whose first word is err) carries the stream-K scratch
+  const TcPlan p = tc_plan((int64_t)s.m_tiles * s.n_tiles, s.k_blocks, tc_nsm());
+  s.sk_tiles = p.sk_tiles;
+  s.seg_max = p.seg_max;
+  s.counters = reinterpret_cast<int*>(reinterpret_cast<char*>(err) + WS_HEADER);
+  s.part = reinterpret_cast<float*>(reinterpret_cast<char*>(err) + WS_HEADER + TC_SK_COUNTER_BYTES);
   return s;
 }
 
@@ -188,9 +259,7 @@ cudaError_t launch_tc(int kid, const CUtensorMap& ta, const CUtensorMap& tb, con
   constexpr int smem = TcSmem<TC_BN, TC_STAGES>::DYN_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int tiles = s.m_tiles * s.n_tiles;
-  const int nsm = sm_count();
-  const int grid = tiles < nsm ? tiles : nsm;
+  const int grid = tc_plan((int64_t)s.m_tiles * s.n_tiles, s.k_blocks, tc_nsm()).grid;
   ProfScope prof(kid, st);
   kern<<<grid, TC_THREADS, smem, st>>>(ta, tb, s, ep);
   g_last_launches.fetch_add(1);
@@ -535,6 +604,8 @@ size_t swiglu_mlp_workspace_bytes(int64_t M, int64_t D, int64_t H, swiglu_dtype 
     const NgPlan p = ng_plan(M, D, H);
     return WS_HEADER + p.counter_bytes + p.part_bytes;
   }
+  if (dtype == SWIGLU_BF16 || dtype == SWIGLU_F16)
+    return WS_HEADER + TC_SK_COUNTER_BYTES + tc_ws_part_bytes(M, D, H, op);
   return WS_HEADER;
 }
 
@@ -548,7 +619,7 @@ swiglu_status swiglu_mlp_fwd(const void* X, const void* Wgu, const void* Wd, voi
   if ((st = check_ptrs({X, Wgu, Wd, Y, saved})) != SWIGLU_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(ws);
-  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
+  if (cudaMemsetAsync(err, 0, ws_clear_bytes(dtype), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
   const size_t e = elt_bytes(dtype);
   char* sv = static_cast<char*>(saved);
   void* G = sv;
@@ -580,7 +651,7 @@ swiglu_status swiglu_mlp_fwd_nograd(const void* X, const void* Wgu, const void* 
                                 : ng_forward<false>(X, Wgu, Wd, Y, A, M, D, H, w, s);
   }
   int* err = static_cast<int*>(ws);
-  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
+  if (cudaMemsetAsync(err, 0, ws_clear_bytes(dtype), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
   switch (dtype) {
     case SWIGLU_BF16:
       return tc_forward<true>(X, Wgu, Wd, Y, nullptr, nullptr, 0, A, H, M, D, H, err, s);
@@ -628,7 +699,7 @@ swiglu_status swiglu_mlp_bwd(const void* dY, const void* X, const void* Wgu, con
   if ((st = check_ptrs({dY, X, Wgu, Wd, saved, dX, dWgu, dWd})) != SWIGLU_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(ws);
-  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
+  if (cudaMemsetAsync(err, 0, ws_clear_bytes(dtype), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
   switch (dtype) {
     case SWIGLU_BF16:
       return tc_backward<true>(dY, X, Wgu, Wd, saved, dX, dWgu, dWd, M, D, H, err, s);

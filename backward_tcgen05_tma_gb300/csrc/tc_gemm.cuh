@@ -46,7 +46,75 @@ struct TcShape {
   uint64_t wait_limit_ns;
   int* err;              // device error word (workspace)
   int inject_stall;      // test hook: producer skips stage 0 of its first tile
+  // Stream-K hybrid (sk_tiles = 0: every tile whole, round-robin).  Tiles
+  // [0, sk_tiles) of the raster order are shared: their k-blocks, laid end to
+  // end, are split evenly over the CTAs, which stream their share first; the
+  // remaining tiles are taken whole, round-robin.  A shared tile's segments
+  // leave fp32 partial tiles in `part` (slot = CTA x segment); the last CTA to
+  // finish a shared tile (counter) sums them in CTA order into its TMEM
+  // accumulator and runs the epilogue.
+  int sk_tiles;
+  int seg_max;     // partial slots per CTA
+  float* part;     // [gridDim.x * seg_max][128 * BN] fp32 in TMEM order
+  int* counters;   // [sk_tiles], zero at launch; each reducer re-zeroes its own
 };
+
+// Stream-K partition of `total` shared k-blocks: CTA c owns
+// [sk_start(c), sk_start(c + 1)).
+__device__ __forceinline__ int64_t sk_start(int64_t c, int64_t total, int64_t ctas) {
+  return c * total / ctas;
+}
+
+// The CTA whose stream-K range holds shared k-block x.
+__device__ __forceinline__ int sk_owner(int64_t x, int64_t total, int64_t ctas) {
+  int64_t c = x * ctas / total;
+  while (c + 1 < ctas && sk_start(c + 1, total, ctas) <= x) ++c;
+  while (c > 0 && sk_start(c, total, ctas) > x) --c;
+  return (int)c;
+}
+
+// One CTA's work: its stream-K range over the shared tiles, then its whole
+// tiles (sk_tiles + blockIdx.x, + gridDim.x, ...).
+struct TcSegIter {
+  int64_t x, x_end;  // shared k-blocks still to cover
+  int kb_tile;
+  int t, tiles, step;
+  __device__ __forceinline__ bool next(int& tile, int& kb0, int& nkb, bool& whole) {
+    if (x < x_end) {
+      tile = (int)(x / kb_tile);
+      kb0 = (int)(x - (int64_t)tile * kb_tile);
+      nkb = (int)min((int64_t)(kb_tile - kb0), x_end - x);
+      x += nkb;
+      whole = false;
+      return true;
+    }
+    if (t < tiles) {
+      tile = t;
+      kb0 = 0;
+      nkb = kb_tile;
+      t += step;
+      whole = true;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Named barrier 1 over the 256 epilogue threads; the AND form returns the
+// same decision to every one of them.
+__device__ __forceinline__ void tc_epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ int tc_epi_bar_and(int v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(v)
+      : "memory");
+  return r;
+}
 
 // Tile order: groups of group_m m-tiles, m fastest inside a group, so the CTAs
 // running at one time share a few A row-blocks and B column-blocks in L2.
@@ -392,6 +460,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int num_tiles = s.m_tiles * s.n_tiles;
+  const int64_t sk_total = (int64_t)s.sk_tiles * s.k_blocks;  // shared k-blocks
+  const int64_t ctas = gridDim.x;
+  auto segs = [&]() {
+    return TcSegIter{sk_start(blockIdx.x, sk_total, ctas), sk_start(blockIdx.x + 1, sk_total, ctas),
+                     s.k_blocks, s.sk_tiles + (int)blockIdx.x, num_tiles, (int)gridDim.x};
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -401,11 +475,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       uint32_t issued_mask = 0, issued_parity = 0;  // last load per stage
       bool ok = true;
       bool skip_once = s.inject_stall != 0;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      TcSegIter it = segs();
+      int tile, kb0, nkb;
+      bool whole;
+      while (ok && it.next(tile, kb0, nkb, whole)) {
         int mt, nt;
-        tc_tile_coords(t, s, mt, nt);
+        tc_tile_coords(tile, s, mt, nt);
         const int m0 = mt * TC_BM;
-        for (int kb = 0; kb < s.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb0 + nkb; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s.wait_limit_ns, abort_flag, s.err)) {
             ok = false;
             break;
@@ -460,14 +537,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      TcSegIter it = segs();
+      int tile, kb0, nkb;
+      bool whole;
+      while (ok && it.next(tile, kb0, nkb, whole)) {
         if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, s.wait_limit_ns, abort_flag, s.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < s.k_blocks; ++kb) {
+        for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded(full_bar(stage), phase, s.wait_limit_ns, abort_flag, s.err)) {
             ok = false;
             break;
@@ -507,21 +587,104 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;  // column half of the tile
     const int row = quarter * 32 + lane;
+    const int e = threadIdx.x - 64;  // 0..255 among the epilogue threads
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFFSET + 8);
+    constexpr int CH = BN / 64;      // 32-column chunks per half
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-      // one lane waits and the warp follows it: tcgen05.ld is warp-aligned
+    int seg = 0;  // shared segments done (= partial slot index)
+    TcSegIter it = segs();
+    int tile, kb0, nkb;
+    bool whole;
+    while (it.next(tile, kb0, nkb, whole)) {
+      // one lane per warp waits; all eight warps then take the same branch
       int ok = 1;
       if (lane == 0)
         ok = mbar_wait_bounded(accf_bar(acc), acc_phase, s.wait_limit_ns, abort_flag, s.err) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      if (!tc_epi_bar_and(ok)) break;
       tc_fence_after();
       int mt, nt;
-      tc_tile_coords(t, s, mt, nt);
+      tc_tile_coords(tile, s, mt, nt);
       const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      Epi::template run<BN, BF16>(ep, s, tacc, mt * TC_BM, nt, row, half,
-                                  smem + L::EPI_OFFSET + (warp - 2) * 2048);
+      int run_epi = whole ? 1 : 0;
+      if (!whole) {
+        // partial tile -> this CTA's slot, in TMEM order (coalesced: lanes
+        // of a warp write consecutive 16-byte groups)
+        float4* slot = reinterpret_cast<float4*>(
+            s.part + ((size_t)blockIdx.x * s.seg_max + seg) * (size_t)(TC_BM * BN));
+#pragma unroll 1
+        for (int c = half * CH; c < (half + 1) * CH; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tacc + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            slot[((c * 4 + quarter) * 8 + g) * 32 + lane] =
+                make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                            __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+        }
+        __threadfence();
+        ++seg;
+        const int c_first = sk_owner((int64_t)tile * s.k_blocks, sk_total, ctas);
+        const int c_last = sk_owner((int64_t)(tile + 1) * s.k_blocks - 1, sk_total, ctas);
+        tc_epi_bar();
+        if (e == 0) {
+          int last = 0;
+          if (!*abort_flag) last = atomicAdd(s.counters + tile, 1) == c_last - c_first;
+          *last_flag = last;
+        }
+        tc_epi_bar();
+        run_epi = *last_flag;
+        if (run_epi) {
+          // the last CTA: sum every partial of the tile in CTA order (its own
+          // straight from TMEM) and put the sum back into its accumulator
+          __threadfence();
+#pragma unroll 1
+          for (int c = half * CH; c < (half + 1) * CH; ++c) {
+            uint32_t own[32];
+            tmem_ld_32x32b_x32(tacc + c * 32, own);
+            tmem_ld_wait();
+            float sum[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sum[i] = 0.0f;
+#pragma unroll 1
+            for (int pc = c_first; pc <= c_last; ++pc) {
+              if (pc == (int)blockIdx.x) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sum[i] += __uint_as_float(own[i]);
+              } else {
+                const int j = tile - (int)(sk_start(pc, sk_total, ctas) / s.k_blocks);
+                const float4* ps = reinterpret_cast<const float4*>(
+                    s.part + ((size_t)pc * s.seg_max + j) * (size_t)(TC_BM * BN));
+                float4 v[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) v[g] = __ldcg(ps + ((c * 4 + quarter) * 8 + g) * 32 + lane);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                  sum[4 * g] += v[g].x;
+                  sum[4 * g + 1] += v[g].y;
+                  sum[4 * g + 2] += v[g].z;
+                  sum[4 * g + 3] += v[g].w;
+                }
+              }
+            }
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(sum[i]);
+            tmem_st_32x32b_x32(tacc + c * 32, w);
+          }
+          tmem_st_wait();
+          if (e == 0) s.counters[tile] = 0;  // ready for the next launch
+          // the epilogue may read columns that another thread summed
+          tc_fence_before();
+          tc_epi_bar();
+          tc_fence_after();
+        }
+      }
+      if (run_epi)
+        Epi::template run<BN, BF16>(ep, s, tacc, mt * TC_BM, nt, row, half,
+                                    smem + L::EPI_OFFSET + (warp - 2) * 2048);
       tc_fence_before();
       mbar_arrive(acce_bar(acc));
       if (++acc == 2) {

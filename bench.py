@@ -212,7 +212,9 @@ def _alloc(M, D, H, dt, device):
          "dX": torch.empty(M, D, dtype=dt, device=device),
          "dWgu": torch.empty(2 * H, D, dtype=dt, device=device),
          "dWd": torch.empty(D, H, dtype=dt, device=device)}
-    e["ws"] = api.workspace(M, D, H, dt, api.SWIGLU_OP_BWD, device)
+    e["ws"] = torch.zeros(max(api.lib().swiglu_mlp_workspace_bytes(M, D, H, api.dtype_code(dt), op)
+                              for op in (api.SWIGLU_OP_FWD, api.SWIGLU_OP_BWD)),
+                          dtype=torch.uint8, device=device)
     return e
 
 

@@ -40,12 +40,15 @@
  * nothing.  ``stream`` is a cudaStream_t (0 = legacy default stream).
  *
  * Workspace: ``ws`` is a device buffer of at least swiglu_mlp_workspace_bytes()
- * bytes, owned by the caller, ZERO-FILLED before its first use.  The library
- * keeps a device error word in it (cleared at the start of every call) and,
- * for the few-token no-grad path, per-tile counters (left at zero by every
- * completed call) and fp32 partial sums.  After a SWIGLU_ERR_DEVICE_TIMEOUT,
- * zero-fill it again before reuse.  Calls that share one workspace must not
- * overlap on the GPU.  The library itself allocates no memory.
+ * bytes (a size for the current device), owned by the caller, ZERO-FILLED
+ * before its first use.  It holds a device error word (cleared at the start
+ * of every call), per-tile arrival counters (cleared by every training call,
+ * left at zero by every completed few-token no-grad call) and fp32 partial
+ * tiles: when a GEMM's last round of whole tiles would leave SMs idle, its
+ * remaining tiles are split along K over all SMs (stream-K) and the partial
+ * sums meet in the workspace.  After a SWIGLU_ERR_DEVICE_TIMEOUT, zero-fill
+ * it again before reuse.  Calls that share one workspace must not overlap on
+ * the GPU.  The library itself allocates no memory.
  *
  * Calls are asynchronous on ``stream`` and do not synchronise (except
  * swiglu_mlp_query_error).  Argument errors are detected on the host before

@@ -51,7 +51,10 @@ P_MIS = ctypes.c_void_p(0x10002)
 N = ctypes.c_void_p(0)
 
 
-def _fwd(L, X=P, W=P, Wd=P, Y=P, S=P, M=128, D=64, H=128, dt=0, ws=P, wsb=256):
+BIG = 1 << 30  # more workspace than any call here needs (never dereferenced)
+
+
+def _fwd(L, X=P, W=P, Wd=P, Y=P, S=P, M=128, D=64, H=128, dt=0, ws=P, wsb=BIG):
     return L.swiglu_mlp_fwd(X, W, Wd, Y, S, M, D, H, dt, ws, wsb, N)
 
 
@@ -70,14 +73,19 @@ def test_argument_errors_are_reported_before_any_launch(L):
     assert _fwd(L, M=2 ** 31) == UNSUP
     assert L.swiglu_mlp_fwd_nograd(N, P, P, P, P, 4, 64, 128, 0, P, 1 << 30, N) == INVALID
     assert L.swiglu_mlp_fwd_nograd(P, P, P, P, P, 4, 64, 128, 0, P, 256, N) == WSERR
-    assert L.swiglu_mlp_bwd(P, P, P, P, P, P, P, N, 4, 64, 128, 0, P, 256, N) == INVALID
-    assert L.swiglu_mlp_bwd(P, P, P, P, P, P, P, P_MIS, 4, 64, 128, 0, P, 256, N) == ALIGN
+    assert L.swiglu_mlp_bwd(P, P, P, P, P, P, P, N, 4, 64, 128, 0, P, BIG, N) == INVALID
+    assert L.swiglu_mlp_bwd(P, P, P, P, P, P, P, P_MIS, 4, 64, 128, 0, P, BIG, N) == ALIGN
+    # the workspace must hold the error word, the shared-tile counters and the
+    # stream-K partial tiles
+    need = L.swiglu_mlp_workspace_bytes(128, 64, 128, 0, 0)
+    assert need > 256
+    assert _fwd(L, wsb=need - 1) == WSERR
 
 
 def test_empty_batch_is_ok_without_launch(L):
     assert _fwd(L, M=0) == OK
-    assert L.swiglu_mlp_fwd_nograd(P, P, P, P, P, 0, 64, 128, 0, P, 256, N) == OK
-    assert L.swiglu_mlp_bwd(P, P, P, P, P, P, P, P, 0, 64, 128, 1, P, 256, N) == OK
+    assert L.swiglu_mlp_fwd_nograd(P, P, P, P, P, 0, 64, 128, 0, P, BIG, N) == OK
+    assert L.swiglu_mlp_bwd(P, P, P, P, P, P, P, P, 0, 64, 128, 1, P, BIG, N) == OK
     assert L.swiglu_mlp_last_launch_count() == 0
 
 

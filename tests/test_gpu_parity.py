@@ -298,3 +298,16 @@ def test_nograd_small_m_parity(M, dtn):
     assert oracle.rel_frob(f64(A), r["A"]) <= TOL[dtn]
     assert within_ulp_frac(f64(A), r["A"], dtn) >= 0.99
     assert oracle.rel_frob(f64(Y), f64(Yt)) <= TOL[dtn]
+
+
+def test_stream_k_shared_tiles_parity_and_determinism():
+    """M=1024, D=512, H=1024 puts every tensor-core GEMM on the stream-K path
+    (fewer tiles than SMs: each tile's k-blocks shared by several CTAs, fp32
+    partials summed by the last one); results must match the oracle and be
+    bitwise reproducible."""
+    t = synthetic.make_inputs(1024, 512, 1024, "bf16", seed=12, device="cuda")
+    a = run_gpu(t, "bf16")
+    b = run_gpu(t, "bf16")
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k])
+    check_all(a, run_oracle(t, "bf16"), "bf16")
