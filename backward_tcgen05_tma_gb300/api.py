@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.swiglu_mlp_inject_stall_once.argtypes = [ci]
         L.swiglu_mlp_last_launch_count.restype = ci
         L.swiglu_mlp_last_launch_count.argtypes = []
+        L.swiglu_mlp_set_cta_pairs.restype = ci
+        L.swiglu_mlp_set_cta_pairs.argtypes = [ci]
         L.swiglu_mlp_profile_enable.restype = None
         L.swiglu_mlp_profile_enable.argtypes = [ci]
         L.swiglu_mlp_profile_read.restype = ci
@@ -219,6 +221,12 @@ def swiglu_mlp_inject_stall_once(on: bool = True) -> None:
 
 def swiglu_mlp_last_launch_count() -> int:
     return int(lib().swiglu_mlp_last_launch_count())
+
+
+def swiglu_mlp_set_cta_pairs(on: bool = True) -> bool:
+    """Tensor-core GEMMs on SM pairs (True, default) or single SMs; returns the
+    previous setting."""
+    return bool(lib().swiglu_mlp_set_cta_pairs(1 if on else 0))
 
 
 def swiglu_mlp_profile_enable(on: bool = True) -> None:

@@ -9,7 +9,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 SO = os.path.join(HERE, "libswiglu_mlp.so")
 SOURCES = ["swiglu_mlp.cu"]
-HEADERS = ["sm103_ptx.cuh", "tc_gemm.cuh", "simt_gemm.cuh", "ng_gemm.cuh"]
+HEADERS = ["sm103_ptx.cuh", "tc_gemm.cuh", "tc2_gemm.cuh", "simt_gemm.cuh", "ng_gemm.cuh"]
 
 NVCC_FLAGS = [
     "-std=c++17", "-O3", "-lineinfo",

@@ -22,6 +22,7 @@
 #include "../../include/swiglu_mlp.h"
 #include "ng_gemm.cuh"
 #include "simt_gemm.cuh"
+#include "tc2_gemm.cuh"
 #include "tc_gemm.cuh"
 
 using namespace swiglu;
@@ -37,6 +38,8 @@ std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 swiglu_status cuda_status(cudaError_t e);
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_last_launches{0};
+std::atomic<int> g_cta_pairs{1};  // tensor-core GEMMs on SM pairs (cta_group::2)
+constexpr int TC2_STAGES = 6;
 
 // ---------------------------------------------------------------------------
 // optional per-kernel timing: CUDA events bracket each launch on its stream
@@ -136,14 +139,15 @@ bool encode_2d(CUtensorMap* tm, bool bf16, const void* base, uint64_t inner, uin
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Wgu [2H][D] seen as [2][H][D]: one box brings rows j0.. of Wg and of Wu.
+// Wgu [2H][D] seen as [2][H][D]: one box brings rows j0.. of Wg and of Wu
+// (depth 2), or of one of them (depth 1: the two CTAs of a pair each bring one).
 bool encode_gateup(CUtensorMap* tm, bool bf16, const void* Wgu, uint64_t D, uint64_t H,
-                   uint32_t rows) {
+                   uint32_t rows, uint32_t depth = 2) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {D, H, 2};
   cuuint64_t strides[2] = {D * 2, H * D * 2};
-  cuuint32_t box[3] = {64, rows, 2};
+  cuuint32_t box[3] = {64, rows, depth};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
              const_cast<void*>(Wgu), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -207,6 +211,44 @@ int tc_nsm() {
   return n < 1 ? 1 : (n > TC_SK_MAX_SMS ? TC_SK_MAX_SMS : n);
 }
 
+// Pairs of SMs that can hold a pair kernel's cluster at once (each TPC
+// whose two SMs are both usable), queried once per device.
+int tc2_units() {
+  static std::mutex mu;
+  static int cached[64];
+  static bool done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> g(mu);
+  if (!done[dev]) {
+    int n = 0;
+    auto kern = tc2_gemm_kernel<TC2_STAGES, LOAD_KMAJOR, LOAD_KMAJOR, true, EpiStore>;
+    constexpr int smem = Tc2Smem<TC2_STAGES>::DYN_BYTES;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2);
+      cfg.blockDim = dim3(TC_THREADS);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    const int cap = tc_nsm() / 2;
+    cached[dev] = n < cap ? n : cap;
+    done[dev] = true;
+  }
+  return cached[dev];
+}
+
+bool use_pairs() { return g_cta_pairs.load() != 0 && tc2_units() >= 1; }
+
+// pairs: tiles of 256 rows handed out per CTA pair (tc2_gemm_kernel).
 // Partial-tile bytes a training call needs: its tensor-core GEMMs as
 // (GEMM rows, GEMM columns, columns per tile, K).  Without a device the bound
 // for any GPU of up to 256 SMs (two slots per CTA).
@@ -220,19 +262,25 @@ size_t tc_ws_part_bytes(int64_t M, int64_t D, int64_t H, int op) {
   const int n = op == SWIGLU_OP_BWD ? 4 : 2;
   for (int i = 0; i < n; ++i) {
     const int64_t* g = op == SWIGLU_OP_BWD ? bwd[i] : fwd[i];
-    const int64_t tiles = ((g[0] + TC_BM - 1) / TC_BM) * ((g[1] + g[2] - 1) / g[2]);
-    const size_t b = tc_part_bytes(tc_plan(tiles, (g[3] + TC_BK - 1) / TC_BK, nsm));
-    if (b > best) best = b;
+    const int64_t kb = (g[3] + TC_BK - 1) / TC_BK, nt = (g[1] + g[2] - 1) / g[2];
+    // one SM per CTA, or pairs of SMs (two CTAs, so two slots sets per unit)
+    const size_t b1 = tc_part_bytes(tc_plan(((g[0] + TC_BM - 1) / TC_BM) * nt, kb, nsm));
+    const int units = tc2_units();  // the pair kernel plans with the same count
+    const size_t b2 =
+        units >= 1 ? 2 * tc_part_bytes(tc_plan(((g[0] + TC2_BM - 1) / TC2_BM) * nt, kb, units)) : 0;
+    if (b1 > best) best = b1;
+    if (b2 > best) best = b2;
   }
   return best;
 }
 
-TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err) {
+TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err, bool pairs) {
   TcShape s;
   s.M = (int)M;
   s.N = (int)N;
   s.K = (int)K;
-  s.m_tiles = (int)((M + TC_BM - 1) / TC_BM);
+  const int64_t bm = pairs ? TC2_BM : TC_BM;
+  s.m_tiles = (int)((M + bm - 1) / bm);
   s.n_tiles = (int)((N + n_per_tile - 1) / n_per_tile);
   s.k_blocks = (int)((K + TC_BK - 1) / TC_BK);
   s.group_m = 16;
@@ -240,7 +288,8 @@ TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err
   s.err = err;
   s.inject_stall = g_inject_stall.exchange(0);
   // the workspace (whose first word is err) carries the stream-K scratch
-  const TcPlan p = tc_plan((int64_t)s.m_tiles * s.n_tiles, s.k_blocks, tc_nsm());
+  const TcPlan p = tc_plan((int64_t)s.m_tiles * s.n_tiles, s.k_blocks,
+                           pairs ? tc2_units() : tc_nsm());
   s.sk_tiles = p.sk_tiles;
   s.seg_max = p.seg_max;
   s.counters = reinterpret_cast<int*>(reinterpret_cast<char*>(err) + WS_HEADER);
@@ -264,6 +313,41 @@ cudaError_t launch_tc(int kid, const CUtensorMap& ta, const CUtensorMap& tb, con
   kern<<<grid, TC_THREADS, smem, st>>>(ta, tb, s, ep);
   g_last_launches.fetch_add(1);
   return cudaGetLastError();
+}
+
+// The pair kernel: clusters of two CTAs on the two SMs of a TPC.
+template <int AM, int BMODE, bool BF16, class Epi>
+cudaError_t launch_tc2(int kid, const CUtensorMap& ta, const CUtensorMap& tb, const TcShape& s,
+                       const typename Epi::Params& ep, cudaStream_t st) {
+  auto kern = tc2_gemm_kernel<TC2_STAGES, AM, BMODE, BF16, Epi>;
+  constexpr int smem = Tc2Smem<TC2_STAGES>::DYN_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int units = tc_plan((int64_t)s.m_tiles * s.n_tiles, s.k_blocks, tc2_units()).grid;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * units));
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ProfScope prof(kid, st);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, s, ep);
+  g_last_launches.fetch_add(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int AM, int BMODE, bool BF16, class Epi>
+cudaError_t launch_gemm(bool pairs, int kid, const CUtensorMap& ta, const CUtensorMap& tb,
+                        const TcShape& s, const typename Epi::Params& ep, cudaStream_t st) {
+  return pairs ? launch_tc2<AM, BMODE, BF16, Epi>(kid, ta, tb, s, ep, st)
+               : launch_tc<AM, BMODE, BF16, Epi>(kid, ta, tb, s, ep, st);
 }
 
 template <bool DUAL, class Epi>
@@ -478,22 +562,26 @@ template <bool BF16>
 swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y, void* G,
                          void* U, int64_t ld_gu, void* A, int64_t ld_a, int64_t M, int64_t D,
                          int64_t H, int* err, cudaStream_t st) {
+  const bool pairs = use_pairs();
+  // a K-major B tile is 256 rows on one SM, 128 rows per CTA on a pair
+  const uint32_t b_rows = pairs ? 128 : TC_BN;
   CUtensorMap tx, tw, ta, twd;
   // gate/up + SwiGLU: C[m, j | H + j], N counts hidden units, BN/2 per tile
-  if (!map_kmajor(&tx, BF16, X, D, M, D, TC_BM) || !encode_gateup(&tw, BF16, Wgu, D, H, TC_BN / 2))
+  if (!map_kmajor(&tx, BF16, X, D, M, D, TC_BM) ||
+      !encode_gateup(&tw, BF16, Wgu, D, H, TC_BN / 2, pairs ? 1 : 2))
     return SWIGLU_ERR_CUDA;
-  TcShape s1 = make_shape(M, H, D, TC_BN / 2, err);
+  TcShape s1 = make_shape(M, H, D, TC_BN / 2, err, pairs);
   EpiSwiGLU::Params p1{G, U, ld_gu, A, ld_a};
-  cudaError_t e = launch_tc<LOAD_KMAJOR, LOAD_GATEUP, BF16, EpiSwiGLU>(
-      G != nullptr ? K_GATE_UP : K_GATE_UP_NOGRAD, tx, tw, s1, p1, st);
+  cudaError_t e = launch_gemm<LOAD_KMAJOR, LOAD_GATEUP, BF16, EpiSwiGLU>(
+      pairs, G != nullptr ? K_GATE_UP : K_GATE_UP_NOGRAD, tx, tw, s1, p1, st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   // down projection: Y = A Wd^T
-  if (!map_kmajor(&ta, BF16, A, H, M, ld_a, TC_BM) || !map_kmajor(&twd, BF16, Wd, H, D, H, TC_BN))
+  if (!map_kmajor(&ta, BF16, A, H, M, ld_a, TC_BM) || !map_kmajor(&twd, BF16, Wd, H, D, H, b_rows))
     return SWIGLU_ERR_CUDA;
-  TcShape s2 = make_shape(M, D, H, TC_BN, err);
+  TcShape s2 = make_shape(M, D, H, TC_BN, err, pairs);
   EpiStore::Params p2{Y, D};
-  return cuda_status(launch_tc<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore>(
-      G != nullptr ? K_DOWN : K_DOWN_NOGRAD, ta, twd, s2, p2, st));
+  return cuda_status(launch_gemm<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore>(
+      pairs, G != nullptr ? K_DOWN : K_DOWN_NOGRAD, ta, twd, s2, p2, st));
 }
 
 template <bool BF16>
@@ -505,42 +593,43 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   void* G = sv;
   void* U = sv + H * 2;
   void* A = sv + 2 * H * 2;
+  const bool pairs = use_pairs();
   CUtensorMap m1, m2;
   cudaError_t e;
   // dWd [D, H] = dY^T A: both operands MN-major over the token dimension
   if (!map_mnmajor(&m1, BF16, dY, D, M, D) || !map_mnmajor(&m2, BF16, A, H, M, ld))
     return SWIGLU_ERR_CUDA;
   {
-    TcShape s = make_shape(D, H, M, TC_BN, err);
+    TcShape s = make_shape(D, H, M, TC_BN, err, pairs);
     EpiStore::Params p{dWd, H};
-    e = launch_tc<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DWD, m1, m2, s, p, st);
+    e = launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWD, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   // dA = dY Wd (Wd read MN-major as [K = D][N = H]); dG, dU written over G, U
   if (!map_kmajor(&m1, BF16, dY, D, M, D, TC_BM) || !map_mnmajor(&m2, BF16, Wd, H, D, H))
     return SWIGLU_ERR_CUDA;
   {
-    TcShape s = make_shape(M, H, D, TC_BN, err);
+    TcShape s = make_shape(M, H, D, TC_BN, err, pairs);
     EpiDSwiGLU::Params p{G, U, ld};
-    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLU>(K_DGU, m1, m2, s, p, st);
+    e = launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLU>(pairs, K_DGU, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   // [dWg; dWu] [2H, D] = [dG | dU]^T X: one GEMM over the 2H columns
   if (!map_mnmajor(&m1, BF16, G, 2 * H, M, ld) || !map_mnmajor(&m2, BF16, X, D, M, D))
     return SWIGLU_ERR_CUDA;
   {
-    TcShape s = make_shape(2 * H, D, M, TC_BN, err);
+    TcShape s = make_shape(2 * H, D, M, TC_BN, err, pairs);
     EpiStore::Params p{dWgu, D};
-    e = launch_tc<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DWGU, m1, m2, s, p, st);
+    e = launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWGU, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   // dX [M, D] = [dG | dU] [Wg; Wu]: K = 2H in one accumulator
   if (!map_kmajor(&m1, BF16, G, 2 * H, M, ld, TC_BM) || !map_mnmajor(&m2, BF16, Wgu, D, 2 * H, D))
     return SWIGLU_ERR_CUDA;
   {
-    TcShape s = make_shape(M, D, 2 * H, TC_BN, err);
+    TcShape s = make_shape(M, D, 2 * H, TC_BN, err, pairs);
     EpiStore::Params p{dX, D};
-    e = launch_tc<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(K_DX, m1, m2, s, p, st);
+    e = launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DX, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   return SWIGLU_OK;
@@ -744,6 +833,8 @@ uint64_t swiglu_mlp_set_wait_limit_ns(uint64_t ns) {
 void swiglu_mlp_inject_stall_once(int on) { g_inject_stall.store(on ? 1 : 0); }
 
 int swiglu_mlp_last_launch_count(void) { return g_last_launches.load(); }
+
+int swiglu_mlp_set_cta_pairs(int on) { return g_cta_pairs.exchange(on ? 1 : 0); }
 
 void swiglu_mlp_profile_enable(int on) { g_prof_on.store(on ? 1 : 0); }
 

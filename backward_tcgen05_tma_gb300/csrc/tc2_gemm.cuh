@@ -1,0 +1,344 @@
+// tc2_gemm.cuh -- the tensor-core GEMM on SM pairs (tcgen05 cta_group::2).
+//
+// A cluster of two CTAs on the two SMs of a TPC computes 256 x 256 output
+// tiles with one tcgen05.mma.cta_group::2 M=256 N=256 K=16 per step, issued
+// by the even CTA.  Each CTA's shared memory holds its own 128 rows of A and
+// its own half (128 of the 256 columns) of B, loaded by its own TMA; each
+// CTA's TMEM holds its 128 rows of the accumulator.  Per SM and k-block that
+// is 32 KB of operands instead of the 48 KB of a 128 x 256 single-SM tile for
+// the same tensor-core work, which relieves the shared-memory port that both
+// TMA writes and MMA operand reads go through.
+//
+// Roles, per CTA (10 warps as in tc_gemm.cuh):
+//   warp 0      TMA producer (both CTAs): waits for its own ring slot to be
+//               free (the MMA's commit reaches both CTAs), loads its halves,
+//               and counts the bytes on the even CTA's "full" barrier;
+//   warp 1      both CTAs allocate TMEM for the pair; the even CTA issues the
+//               MMAs and commits to both CTAs' "empty" / "accumulator full"
+//               barriers;
+//   warps 2..9  epilogue of this CTA's 128 rows (the epilogues of
+//               tc_gemm.cuh, unchanged); one arrival per warp on the even
+//               CTA's "accumulator empty" barrier.
+// Tiles (and the stream-K shares of the hybrid) are handed out per cluster.
+#pragma once
+
+#include "tc_gemm.cuh"
+
+namespace swiglu {
+
+constexpr int TC2_BM = 256;  // output rows per tile (128 per CTA)
+constexpr int TC2_BN = 256;
+
+template <int STAGES>
+struct Tc2Smem {
+  static constexpr int A_BYTES = 128 * TC_BK * 2;  // this CTA's 128 rows of A
+  static constexpr int B_BYTES = 128 * TC_BK * 2;  // this CTA's 128 columns of B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;  // 8 warps x 2 KB store staging
+  static constexpr int BAR_OFFSET = EPI_OFFSET + 8 * 2048;
+  // barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int MISC_OFFSET = BAR_OFFSET + NUM_BARS * 8;  // tmem slot, abort, last
+  static constexpr int TOTAL = MISC_OFFSET + 16;
+  static constexpr int DYN_BYTES = TOTAL + 1024;
+  static constexpr int TMEM_COLS = 2 * TC2_BN;
+};
+
+template <int STAGES, int A_MODE, int B_MODE, bool BF16, class Epi>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const TcShape s,
+                    const typename Epi::Params ep) {
+  using L = Tc2Smem<STAGES>;
+  constexpr int BN = TC2_BN;
+  static_assert(L::TOTAL + 1024 <= 232448, "shared memory plan exceeds 227 KB");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::BAR_OFFSET;
+  auto full_bar = [&](int i) { return bar0 + 8u * i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (STAGES + i); };
+  auto accf_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + i); };
+  auto acce_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 + i); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFFSET);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFFSET + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFFSET + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: the CTA that issues the MMAs
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(accf_bar(i), 1);
+      mbar_init(acce_bar(i), 16);  // one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_cg2(smem_u32(tmem_slot), L::TMEM_COLS);
+    tmem_relinquish_cg2();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = s.m_tiles * s.n_tiles;
+  const int64_t sk_total = (int64_t)s.sk_tiles * s.k_blocks;
+  const int cl = (int)(blockIdx.x >> 1);
+  const int64_t ncl = gridDim.x >> 1;
+  auto segs = [&]() {
+    return TcSegIter{sk_start(cl, sk_total, ncl), sk_start(cl + 1, sk_total, ncl), s.k_blocks,
+                     s.sk_tiles + cl, num_tiles, (int)ncl};
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      bool skip_once = s.inject_stall != 0 && leader;
+      TcSegIter it = segs();
+      int tile, kb0, nkb;
+      bool whole;
+      while (ok && it.next(tile, kb0, nkb, whole)) {
+        int mt, nt;
+        tc_tile_coords(tile, s, mt, nt);
+        const int m0 = mt * TC2_BM + (int)rank * 128;  // this CTA's rows of A
+        const int nb = nt * BN + (int)rank * 128;      // this CTA's columns of B
+        for (int kb = kb0; kb < kb0 + nkb; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s.wait_limit_ns, abort_flag, s.err)) {
+            ok = false;
+            break;
+          }
+          if (skip_once) {
+            skip_once = false;  // fault injection: this stage never fills
+          } else {
+            const uint32_t sa = sbase + stage * L::STAGE_BYTES;
+            const uint32_t sb = sa + L::A_BYTES;
+            const uint32_t fb = mapa_shared(full_bar(stage), 0);
+            const int k0 = kb * TC_BK;
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * L::STAGE_BYTES);
+            if (A_MODE == LOAD_KMAJOR) {
+              tma_load_2d_cg2(sa, &tmA, fb, k0, m0);
+            } else {
+              tma_load_2d_cg2(sa, &tmA, fb, m0, k0);
+              tma_load_2d_cg2(sa + 8192, &tmA, fb, m0 + 64, k0);
+            }
+            if (B_MODE == LOAD_KMAJOR) {
+              tma_load_2d_cg2(sb, &tmB, fb, k0, nb);
+            } else if (B_MODE == LOAD_GATEUP) {
+              // the even CTA brings the Wg rows, the odd one the Wu rows
+              tma_load_3d_cg2(sb, &tmB, fb, k0, nt * (BN / 2), (int)rank);
+            } else {
+              tma_load_2d_cg2(sb, &tmB, fb, nb, k0);
+              tma_load_2d_cg2(sb + 8192, &tmB, fb, nb + 64, k0);
+            }
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        // unwinding: the copies counted on this CTA's barriers land first
+        for (int i = 0; i < STAGES; ++i)
+          if (issued_mask & (1u << i))
+            mbar_wait_bounded(full_bar(i), (issued_parity >> i) & 1u, s.wait_limit_ns, nullptr,
+                              s.err);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc =
+          make_idesc_f16(BF16, A_MODE == LOAD_MNMAJOR, B_MODE == LOAD_MNMAJOR, TC2_BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      TcSegIter it = segs();
+      int tile, kb0, nkb;
+      bool whole;
+      while (ok && it.next(tile, kb0, nkb, whole)) {
+        if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, s.wait_limit_ns, abort_flag, s.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, s.wait_limit_ns, abort_flag, s.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sbase + stage * L::STAGE_BYTES;
+          const uint32_t sb = sa + L::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < TC_BK / TC_UMMA_K; ++kk) {
+            const uint64_t ad = (A_MODE == LOAD_MNMAJOR)
+                                    ? make_sw128_desc(sa + kk * 2048, 8192, 1024)
+                                    : make_sw128_desc(sa + kk * 32, 16, 1024);
+            const uint64_t bd = (B_MODE == LOAD_MNMAJOR)
+                                    ? make_sw128_desc(sb + kk * 2048, 8192, 1024)
+                                    : make_sw128_desc(sb + kk * 32, 16, 1024);
+            umma_f16_ss_cg2(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit_cg2_mc(empty_bar(stage), 0x3);  // frees the slot in both CTAs
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_cg2_mc(accf_bar(acc), 0x3);  // accumulator complete in both CTAs
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      umma_commit_cg2_mc(drain_bar, 0x1);
+      mbar_wait_bounded(drain_bar, 0, s.wait_limit_ns, nullptr, s.err);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // column half of the tile
+    const int row = quarter * 32 + lane;
+    const int e = threadIdx.x - 64;  // 0..255 among the epilogue threads
+    constexpr int CH = BN / 64;      // 32-column chunks per half
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int seg = 0;  // shared segments done (= partial slot index)
+    TcSegIter it = segs();
+    int tile, kb0, nkb;
+    bool whole;
+    while (it.next(tile, kb0, nkb, whole)) {
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_wait_bounded(accf_bar(acc), acc_phase, s.wait_limit_ns, abort_flag, s.err) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!tc_epi_bar_and(ok)) break;
+      tc_fence_after();
+      int mt, nt;
+      tc_tile_coords(tile, s, mt, nt);
+      const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      int run_epi = whole ? 1 : 0;
+      if (!whole) {
+        // this CTA's 128 rows of the partial tile -> its slot, in TMEM order
+        float4* slot = reinterpret_cast<float4*>(
+            s.part + ((size_t)blockIdx.x * s.seg_max + seg) * (size_t)(TC_BM * BN));
+#pragma unroll 1
+        for (int c = half * CH; c < (half + 1) * CH; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tacc + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            slot[((c * 4 + quarter) * 8 + g) * 32 + lane] =
+                make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                            __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+        }
+        __threadfence();
+        ++seg;
+        // clusters sharing this tile; each CTA half of the tile has its own counter
+        const int c_first = sk_owner((int64_t)tile * s.k_blocks, sk_total, ncl);
+        const int c_last = sk_owner((int64_t)(tile + 1) * s.k_blocks - 1, sk_total, ncl);
+        tc_epi_bar();
+        if (e == 0) {
+          int last = 0;
+          if (!*abort_flag) last = atomicAdd(s.counters + 2 * tile + rank, 1) == c_last - c_first;
+          *last_flag = last;
+        }
+        tc_epi_bar();
+        run_epi = *last_flag;
+        if (run_epi) {
+          __threadfence();
+#pragma unroll 1
+          for (int c = half * CH; c < (half + 1) * CH; ++c) {
+            uint32_t own[32];
+            tmem_ld_32x32b_x32(tacc + c * 32, own);
+            tmem_ld_wait();
+            float sum[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sum[i] = 0.0f;
+#pragma unroll 1
+            for (int pc = c_first; pc <= c_last; ++pc) {
+              if (pc == cl) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sum[i] += __uint_as_float(own[i]);
+              } else {
+                const int j = tile - (int)(sk_start(pc, sk_total, ncl) / s.k_blocks);
+                const float4* ps = reinterpret_cast<const float4*>(
+                    s.part + ((size_t)(2 * pc + rank) * s.seg_max + j) * (size_t)(TC_BM * BN));
+                float4 v[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) v[g] = __ldcg(ps + ((c * 4 + quarter) * 8 + g) * 32 + lane);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                  sum[4 * g] += v[g].x;
+                  sum[4 * g + 1] += v[g].y;
+                  sum[4 * g + 2] += v[g].z;
+                  sum[4 * g + 3] += v[g].w;
+                }
+              }
+            }
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(sum[i]);
+            tmem_st_32x32b_x32(tacc + c * 32, w);
+          }
+          tmem_st_wait();
+          if (e == 0) s.counters[2 * tile + rank] = 0;  // ready for the next launch
+          tc_fence_before();
+          tc_epi_bar();
+          tc_fence_after();
+        }
+      }
+      if (run_epi)
+        Epi::template run<BN, BF16>(ep, s, tacc, mt * TC2_BM + (int)rank * 128, nt, row, half,
+                                    smem + L::EPI_OFFSET + (warp - 2) * 2048);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the pair frees its TMEM together, after both are done
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_cg2(tmem_base, L::TMEM_COLS);
+  }
+}
+
+}  // namespace swiglu

@@ -89,8 +89,16 @@ def test_tiny_fp32_ieee_parity():
         assert oracle.rel_frob(g[k], r[k]) <= 1e-6, k
 
 
+@pytest.fixture(params=[True, False], ids=["sm_pairs", "single_sm"])
+def cta_pairs(request):
+    """Runs a test with the tensor-core GEMMs on SM pairs and on single SMs."""
+    old = api.swiglu_mlp_set_cta_pairs(request.param)
+    yield request.param
+    api.swiglu_mlp_set_cta_pairs(old)
+
+
 @pytest.mark.parametrize("dtn", ["bf16", "f16"])
-def test_ragged_multi_tile_parity(dtn):
+def test_ragged_multi_tile_parity(dtn, cta_pairs):
     # 3 row tiles (ragged), 4 gate/up column tiles (ragged), K=2H=784 (ragged k-blocks)
     t = synthetic.make_inputs(333, 320, 392, dtn, seed=3, device="cuda")
     check_all(run_gpu(t, dtn), run_oracle(t, dtn), dtn)
@@ -104,7 +112,7 @@ def test_edge_shapes(M, D, H):
 
 
 @pytest.mark.parametrize("dtn", ["bf16", "f16"])
-def test_exact_accumulation_inputs_bitwise_gate_up(dtn):
+def test_exact_accumulation_inputs_bitwise_gate_up(dtn, cta_pairs):
     """Dyadic-grid inputs make every fp32 partial sum exact, so the GPU's
     accumulators equal the oracle's exact sums: stored G, U must be bitwise
     equal, A and dG/dU within one unit in the last place."""
@@ -202,7 +210,7 @@ def test_device_errors_are_statuses():
     assert api.swiglu_mlp_query_error(ws) == 0
 
 
-def test_stalled_pipeline_times_out_cleanly():
+def test_stalled_pipeline_times_out_cleanly(cta_pairs):
     """Failure detection without a fault: the producer skips one stage, the
     MMA warp's bounded wait runs out, the kernel records a timeout status and
     returns; the context stays usable and the next call is correct."""
@@ -300,7 +308,7 @@ def test_nograd_small_m_parity(M, dtn):
     assert oracle.rel_frob(f64(Y), f64(Yt)) <= TOL[dtn]
 
 
-def test_stream_k_shared_tiles_parity_and_determinism():
+def test_stream_k_shared_tiles_parity_and_determinism(cta_pairs):
     """M=1024, D=512, H=1024 puts every tensor-core GEMM on the stream-K path
     (fewer tiles than SMs: each tile's k-blocks shared by several CTAs, fp32
     partials summed by the last one); results must match the oracle and be
