@@ -223,10 +223,10 @@ def swiglu_mlp_last_launch_count() -> int:
     return int(lib().swiglu_mlp_last_launch_count())
 
 
-def swiglu_mlp_set_cta_pairs(on: bool = True) -> bool:
-    """Tensor-core GEMMs on SM pairs (True, default) or single SMs; returns the
-    previous setting."""
-    return bool(lib().swiglu_mlp_set_cta_pairs(1 if on else 0))
+def swiglu_mlp_set_cta_pairs(mode: int = 1) -> int:
+    """Tensor-core GEMMs on SM pairs: 1 = by size (default), 2 = always,
+    0 = never; returns the previous mode."""
+    return int(lib().swiglu_mlp_set_cta_pairs(int(mode)))
 
 
 def swiglu_mlp_profile_enable(on: bool = True) -> None:

@@ -38,7 +38,7 @@ std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 swiglu_status cuda_status(cudaError_t e);
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_last_launches{0};
-std::atomic<int> g_cta_pairs{1};  // tensor-core GEMMs on SM pairs (cta_group::2)
+std::atomic<int> g_cta_pairs{1};  // SM pairs (cta_group::2): 0 never, 1 by size, 2 always
 constexpr int TC2_STAGES = 6;
 
 // ---------------------------------------------------------------------------
@@ -246,7 +246,19 @@ int tc2_units() {
   return cached[dev];
 }
 
-bool use_pairs() { return g_cta_pairs.load() != 0 && tc2_units() >= 1; }
+// Whether one GEMM runs on SM pairs.  Measured per kernel on GB300: pairs
+// win when the main loop dominates -- long K and several rounds of tiles, or
+// the very long K of the weight gradients -- while short-K GEMMs with heavy
+// epilogues or few tiles run faster on single SMs (the pair's fixed costs and
+// its coupled epilogues are not amortised).
+bool use_pairs(int64_t Mg, int64_t N, int64_t n_per_tile, int64_t K) {
+  const int mode = g_cta_pairs.load();
+  if (mode == 0 || tc2_units() < 1) return false;
+  if (mode == 2) return true;
+  const int64_t tiles = ((Mg + TC_BM - 1) / TC_BM) * ((N + n_per_tile - 1) / n_per_tile);
+  const int64_t kb = (K + TC_BK - 1) / TC_BK;
+  return (kb >= 32 && tiles >= 4 * (int64_t)tc_nsm()) || kb >= 256;
+}
 
 // pairs: tiles of 256 rows handed out per CTA pair (tc2_gemm_kernel).
 // Partial-tile bytes a training call needs: its tensor-core GEMMs as
@@ -562,26 +574,28 @@ template <bool BF16>
 swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y, void* G,
                          void* U, int64_t ld_gu, void* A, int64_t ld_a, int64_t M, int64_t D,
                          int64_t H, int* err, cudaStream_t st) {
-  const bool pairs = use_pairs();
-  // a K-major B tile is 256 rows on one SM, 128 rows per CTA on a pair
-  const uint32_t b_rows = pairs ? 128 : TC_BN;
   CUtensorMap tx, tw, ta, twd;
-  // gate/up + SwiGLU: C[m, j | H + j], N counts hidden units, BN/2 per tile
+  // gate/up + SwiGLU: C[m, j | H + j], N counts hidden units, BN/2 per tile;
+  // on a pair each CTA brings one of Wg, Wu
+  const bool pairs1 = use_pairs(M, H, TC_BN / 2, D);
   if (!map_kmajor(&tx, BF16, X, D, M, D, TC_BM) ||
-      !encode_gateup(&tw, BF16, Wgu, D, H, TC_BN / 2, pairs ? 1 : 2))
+      !encode_gateup(&tw, BF16, Wgu, D, H, TC_BN / 2, pairs1 ? 1 : 2))
     return SWIGLU_ERR_CUDA;
-  TcShape s1 = make_shape(M, H, D, TC_BN / 2, err, pairs);
+  TcShape s1 = make_shape(M, H, D, TC_BN / 2, err, pairs1);
   EpiSwiGLU::Params p1{G, U, ld_gu, A, ld_a};
   cudaError_t e = launch_gemm<LOAD_KMAJOR, LOAD_GATEUP, BF16, EpiSwiGLU>(
-      pairs, G != nullptr ? K_GATE_UP : K_GATE_UP_NOGRAD, tx, tw, s1, p1, st);
+      pairs1, G != nullptr ? K_GATE_UP : K_GATE_UP_NOGRAD, tx, tw, s1, p1, st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
-  // down projection: Y = A Wd^T
-  if (!map_kmajor(&ta, BF16, A, H, M, ld_a, TC_BM) || !map_kmajor(&twd, BF16, Wd, H, D, H, b_rows))
+  // down projection: Y = A Wd^T (a K-major B tile is 256 rows on one SM,
+  // 128 rows per CTA on a pair)
+  const bool pairs2 = use_pairs(M, D, TC_BN, H);
+  if (!map_kmajor(&ta, BF16, A, H, M, ld_a, TC_BM) ||
+      !map_kmajor(&twd, BF16, Wd, H, D, H, pairs2 ? 128 : TC_BN))
     return SWIGLU_ERR_CUDA;
-  TcShape s2 = make_shape(M, D, H, TC_BN, err, pairs);
+  TcShape s2 = make_shape(M, D, H, TC_BN, err, pairs2);
   EpiStore::Params p2{Y, D};
   return cuda_status(launch_gemm<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore>(
-      pairs, G != nullptr ? K_DOWN : K_DOWN_NOGRAD, ta, twd, s2, p2, st));
+      pairs2, G != nullptr ? K_DOWN : K_DOWN_NOGRAD, ta, twd, s2, p2, st));
 }
 
 template <bool BF16>
@@ -593,13 +607,13 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   void* G = sv;
   void* U = sv + H * 2;
   void* A = sv + 2 * H * 2;
-  const bool pairs = use_pairs();
   CUtensorMap m1, m2;
   cudaError_t e;
   // dWd [D, H] = dY^T A: both operands MN-major over the token dimension
   if (!map_mnmajor(&m1, BF16, dY, D, M, D) || !map_mnmajor(&m2, BF16, A, H, M, ld))
     return SWIGLU_ERR_CUDA;
   {
+    const bool pairs = use_pairs(D, H, TC_BN, M);
     TcShape s = make_shape(D, H, M, TC_BN, err, pairs);
     EpiStore::Params p{dWd, H};
     e = launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWD, m1, m2, s, p, st);
@@ -609,6 +623,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   if (!map_kmajor(&m1, BF16, dY, D, M, D, TC_BM) || !map_mnmajor(&m2, BF16, Wd, H, D, H))
     return SWIGLU_ERR_CUDA;
   {
+    const bool pairs = use_pairs(M, H, TC_BN, D);
     TcShape s = make_shape(M, H, D, TC_BN, err, pairs);
     EpiDSwiGLU::Params p{G, U, ld};
     e = launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLU>(pairs, K_DGU, m1, m2, s, p, st);
@@ -618,6 +633,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   if (!map_mnmajor(&m1, BF16, G, 2 * H, M, ld) || !map_mnmajor(&m2, BF16, X, D, M, D))
     return SWIGLU_ERR_CUDA;
   {
+    const bool pairs = use_pairs(2 * H, D, TC_BN, M);
     TcShape s = make_shape(2 * H, D, M, TC_BN, err, pairs);
     EpiStore::Params p{dWgu, D};
     e = launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWGU, m1, m2, s, p, st);
@@ -627,6 +643,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   if (!map_kmajor(&m1, BF16, G, 2 * H, M, ld, TC_BM) || !map_mnmajor(&m2, BF16, Wgu, D, 2 * H, D))
     return SWIGLU_ERR_CUDA;
   {
+    const bool pairs = use_pairs(M, D, TC_BN, 2 * H);
     TcShape s = make_shape(M, D, 2 * H, TC_BN, err, pairs);
     EpiStore::Params p{dX, D};
     e = launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DX, m1, m2, s, p, st);
@@ -834,7 +851,9 @@ void swiglu_mlp_inject_stall_once(int on) { g_inject_stall.store(on ? 1 : 0); }
 
 int swiglu_mlp_last_launch_count(void) { return g_last_launches.load(); }
 
-int swiglu_mlp_set_cta_pairs(int on) { return g_cta_pairs.exchange(on ? 1 : 0); }
+int swiglu_mlp_set_cta_pairs(int mode) {
+  return g_cta_pairs.exchange(mode <= 0 ? 0 : (mode >= 2 ? 2 : 1));
+}
 
 void swiglu_mlp_profile_enable(int on) { g_prof_on.store(on ? 1 : 0); }
 

@@ -194,6 +194,40 @@ __device__ __forceinline__ void warp_store_tile(uint8_t* buf, const uint32_t (&v
   __syncwarp();
 }
 
+// The inverse: a 32 x 32 tile of 16-bit values read with coalesced loads (8
+// rows x 64 contiguous bytes per instruction) and handed to its rows' lanes
+// through the same swizzled 2 KB buffer.  Split in two so the loads of the
+// next tile can be in flight while the current one is used:
+// warp_load_issue (global -> w, zero outside the matrix) and
+// warp_load_finish (w -> the lane's own row, 16 packed words).
+template <class RowPtr, class ChunkOk>
+__device__ __forceinline__ void warp_load_issue(uint4 (&w)[4], int lane, RowPtr row_ptr,
+                                                ChunkOk chunk_ok) {
+  const int q = lane & 3;
+  const bool qok = chunk_ok(q);
+#pragma unroll
+  for (int pass = 0; pass < 4; ++pass) {
+    const uint8_t* src = row_ptr(pass * 8 + (lane >> 2));
+    w[pass] = (src != nullptr && qok) ? *reinterpret_cast<const uint4*>(src + q * 16)
+                                      : make_uint4(0, 0, 0, 0);
+  }
+}
+
+__device__ __forceinline__ void warp_load_finish(uint8_t* buf, const uint4 (&w)[4], int lane,
+                                                 uint4 (&row)[4]) {
+  const int q = lane & 3;
+#pragma unroll
+  for (int pass = 0; pass < 4; ++pass) {
+    const int r = pass * 8 + (lane >> 2);
+    *reinterpret_cast<uint4*>(buf + r * 64 + (q ^ ((r >> 1) & 3)) * 16) = w[pass];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    row[c] = *reinterpret_cast<const uint4*>(buf + lane * 64 + (c ^ ((lane >> 1) & 3)) * 16);
+  __syncwarp();
+}
+
 // sigma(g) = 1 / (1 + e^-g) in fp32 with a correctly rounded reciprocal
 // (exact limits: e^-g = inf gives 0); SiLU(g) = g * sigma(g).
 __device__ __forceinline__ float sigmoid_f32(float g) { return __frcp_rn(1.0f + __expf(-g)); }
@@ -300,48 +334,43 @@ struct EpiDSwiGLU {
     void* u;
     int64_t ld;
   };
-  // G and U of one 32-column chunk of this thread's row (zero outside the
-  // matrix), loaded a chunk ahead so their latency hides behind the math.
-  template <bool BF16>
-  static __device__ __forceinline__ void load_gu(const Params& p, const TcShape& s, int m, int j0,
-                                                 uint4 (&vg)[4], uint4 (&vu)[4]) {
-    using T = typename Pack<BF16>::T;
-    const T* grow = reinterpret_cast<const T*>(p.g) + (int64_t)m * p.ld;
-    const T* urow = reinterpret_cast<const T*>(p.u) + (int64_t)m * p.ld;
-#pragma unroll
-    for (int g8 = 0; g8 < 4; ++g8) {
-      const int j = j0 + g8 * 8;
-      if (m < s.M && j + 8 <= s.N) {
-        vg[g8] = *reinterpret_cast<const uint4*>(grow + j);
-        vu[g8] = *reinterpret_cast<const uint4*>(urow + j);
-      } else {
-        vg[g8] = make_uint4(0, 0, 0, 0);
-        vu[g8] = make_uint4(0, 0, 0, 0);
-      }
-    }
-  }
   template <int BN, bool BF16>
   static __device__ __forceinline__ void run(const Params& p, const TcShape& s, uint32_t tacc,
                                              int m0, int nt, int row, int half, uint8_t* buf) {
     using P = Pack<BF16>;
     using T = typename P::T;
-    const int m = m0 + row;
     const int lane = row & 31;
     const int mw = m0 + (row & ~31);
     const int jt = nt * BN;
     constexpr int CH = BN / 64;  // chunks of 32 columns per half
     const int c0 = half * CH;
-    uint4 ng[4], nu[4];
-    load_gu<BF16>(p, s, m, jt + c0 * 32, ng, nu);
+    auto rows_of = [&](void* base, int jc) {
+      return [=](int rr) -> uint8_t* {
+        const int mm = mw + rr;
+        return mm < s.M ? reinterpret_cast<uint8_t*>(reinterpret_cast<T*>(base) +
+                                                     (int64_t)mm * p.ld + jc)
+                        : nullptr;
+      };
+    };
+    // G and U of the next chunk are loaded (coalesced) while this one is used
+    uint4 wg[4], wu[4];
+    {
+      const int jc = jt + c0 * 32;
+      auto ok = [&](int q) { return jc + q * 8 + 8 <= s.N; };
+      warp_load_issue(wg, lane, rows_of(p.g, jc), ok);
+      warp_load_issue(wu, lane, rows_of(p.u, jc), ok);
+    }
 #pragma unroll 1
     for (int c = c0; c < c0 + CH; ++c) {
       uint4 vg[4], vu[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        vg[q] = ng[q];
-        vu[q] = nu[q];
+      warp_load_finish(buf, wg, lane, vg);
+      warp_load_finish(buf, wu, lane, vu);
+      if (c + 1 < c0 + CH) {
+        const int jn = jt + (c + 1) * 32;
+        auto okn = [&](int q) { return jn + q * 8 + 8 <= s.N; };
+        warp_load_issue(wg, lane, rows_of(p.g, jn), okn);
+        warp_load_issue(wu, lane, rows_of(p.u, jn), okn);
       }
-      if (c + 1 < c0 + CH) load_gu<BF16>(p, s, m, jt + (c + 1) * 32, ng, nu);
       uint32_t r[32];
       tmem_ld_32x32b_x32(tacc + c * 32, r);
       tmem_ld_wait();
@@ -366,22 +395,8 @@ struct EpiDSwiGLU {
       }
       const int jc = jt + c * 32;
       auto ok = [&](int q) { return jc + q * 8 + 8 <= s.N; };
-      warp_store_tile(buf, odg, lane,
-                      [&](int rr) -> uint8_t* {
-                        const int mm = mw + rr;
-                        return mm < s.M ? reinterpret_cast<uint8_t*>(reinterpret_cast<T*>(p.g) +
-                                                                     (int64_t)mm * p.ld + jc)
-                                        : nullptr;
-                      },
-                      ok);
-      warp_store_tile(buf, odu, lane,
-                      [&](int rr) -> uint8_t* {
-                        const int mm = mw + rr;
-                        return mm < s.M ? reinterpret_cast<uint8_t*>(reinterpret_cast<T*>(p.u) +
-                                                                     (int64_t)mm * p.ld + jc)
-                                        : nullptr;
-                      },
-                      ok);
+      warp_store_tile(buf, odg, lane, rows_of(p.g, jc), ok);
+      warp_store_tile(buf, odu, lane, rows_of(p.u, jc), ok);
     }
   }
 };

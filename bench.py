@@ -389,6 +389,8 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     api.lib()
+    if args.cta_pairs is not None:
+        api.swiglu_mlp_set_cta_pairs(args.cta_pairs)
     peaks = _peaks()
     w = WORKLOADS[args.workload]
     M, D, H = w["B"] * w["S"], w["D"], w["H"]
@@ -449,12 +451,15 @@ def run_ours(args):
         extra = {}
         for wl, dts in (("B8_S2048_D1024_H2816", ["bf16"]), ("B8_S4096_D2048_H5632", ["bf16", "f16"])):
             for dn in dts:
-                s2, _, _, keep = _time_training(api, WORKLOADS[wl], dn, 10, 3, 0, device)
+                s2, _, prof2, keep = _time_training(api, WORKLOADS[wl], dn, 10, 3, 0, device,
+                                                    profile=True)
                 del keep
                 w2 = WORKLOADS[wl]
-                f2 = metrics.fwd_bwd_flops(w2["B"] * w2["S"], w2["D"], w2["H"])
-                extra["%s_%s" % (wl, dn)] = {"ms_per_step": round(s2 * 1e3, 3),
-                                             "TFLOPS": round(f2 / s2 / 1e12, 1)}
+                M2, D2, H2 = w2["B"] * w2["S"], w2["D"], w2["H"]
+                f2 = metrics.fwd_bwd_flops(M2, D2, H2)
+                extra["%s_%s" % (wl, dn)] = {
+                    "ms_per_step": round(s2 * 1e3, 3), "TFLOPS": round(f2 / s2 / 1e12, 1),
+                    "kernel_ms": {k: round(v[1] / v[0], 4) for k, v in prof2.items()}}
                 torch.cuda.empty_cache()
         line["other_workloads"] = extra
         line["nograd"] = _nograd_sweep(api, device, peaks)
@@ -480,6 +485,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=MAIN)
     ap.add_argument("--quick", action="store_true", help="main workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cta-pairs", type=int, choices=[0, 1, 2], default=None,
+                    help="tensor-core GEMMs on SM pairs: 1 by size (library default), 2 always, 0 never")
     ap.add_argument("--nograd", default=None,
                     help="comma-separated S values: run only the no-grad sweep (B=1, D=4096, H=11008)")
     args = ap.parse_args()

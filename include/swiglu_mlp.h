@@ -182,13 +182,15 @@ uint64_t swiglu_mlp_set_wait_limit_ns(uint64_t ns);
 void swiglu_mlp_inject_stall_once(int on);
 
 /* Selects how later calls of this process run their bf16/fp16 tensor-core
- * GEMMs: nonzero (the default) on pairs of SMs -- 2-CTA clusters issuing
- * tcgen05.mma.cta_group::2 on 256 x 256 tiles, each SM loading half of each
- * operand tile -- or zero on single SMs (128 x 256 tiles).  Both give results
- * within the same tolerances (the accumulation order differs).  Returns the
- * previous setting.  A workspace sized by swiglu_mlp_workspace_bytes() fits
- * either. */
-int swiglu_mlp_set_cta_pairs(int on);
+ * GEMMs: on pairs of SMs -- 2-CTA clusters issuing tcgen05.mma.cta_group::2
+ * on 256 x 256 tiles, each SM loading half of each operand tile -- or on
+ * single SMs (128 x 256 tiles).  mode 1 (the default): pairs for the GEMMs
+ * whose size favours them (K >= 2048 with at least four rounds of 128 x 256
+ * tiles, or K >= 16384); 2: pairs for every GEMM; 0: never.  All modes give
+ * results within the same tolerances (accumulation order differs).  Returns
+ * the previous mode.  A workspace sized by swiglu_mlp_workspace_bytes() fits
+ * every mode. */
+int swiglu_mlp_set_cta_pairs(int mode);
 
 /* Number of kernels the last fwd / fwd_nograd / bwd call launched on the
  * device (for launch accounting in benchmarks). */
