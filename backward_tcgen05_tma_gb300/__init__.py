@@ -5,4 +5,4 @@ hand-written tcgen05/TMEM/TMA CUDA kernels behind a C ABI
 (``include/swiglu_mlp.h``).  ``backward_tcgen05_tma_gb300.api`` is the thin
 ctypes binding; importing this package does not load the CUDA library.
 """
-__all__ = ["api", "synthetic", "metrics"]
+__all__ = ["api", "module", "synthetic", "metrics"]

@@ -67,6 +67,13 @@ def lib() -> ctypes.CDLL:
         L.swiglu_mlp_fwd_nograd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
         L.swiglu_mlp_fwd_nograd_noalloc.restype = ci
         L.swiglu_mlp_fwd_nograd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
+        L.swiglu_mlp_graph_create_fwd_nograd.restype = ci
+        L.swiglu_mlp_graph_create_fwd_nograd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp,
+                                                         sz, ctypes.POINTER(vp)]
+        L.swiglu_mlp_graph_launch.restype = ci
+        L.swiglu_mlp_graph_launch.argtypes = [vp, vp]
+        L.swiglu_mlp_graph_destroy.restype = ci
+        L.swiglu_mlp_graph_destroy.argtypes = [vp]
         L.swiglu_mlp_bwd.restype = ci
         L.swiglu_mlp_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
         L.swiglu_mlp_query_error.restype = ci
@@ -81,6 +88,8 @@ def lib() -> ctypes.CDLL:
         L.swiglu_mlp_last_launch_count.argtypes = []
         L.swiglu_mlp_set_cta_pairs.restype = ci
         L.swiglu_mlp_set_cta_pairs.argtypes = [ci]
+        L.swiglu_mlp_set_nograd_fused.restype = ci
+        L.swiglu_mlp_set_nograd_fused.argtypes = [ci]
         L.swiglu_mlp_profile_enable.restype = None
         L.swiglu_mlp_profile_enable.argtypes = [ci]
         L.swiglu_mlp_profile_read.restype = ci
@@ -185,6 +194,62 @@ def swiglu_mlp_fwd_nograd_noalloc(X, Wgu, Wd, out: dict | None = None):
     return Y, A
 
 
+class FwdNogradGraph:
+    """A no-grad forward recorded once as a CUDA graph (swiglu_mlp_graph_*)
+    on static buffers ``X`` [M,D], ``Y`` [M,D], ``A`` [M,H] and a workspace;
+    each call copies new tokens into ``X`` (unless they are ``X`` itself),
+    replays the graph on the current stream and returns ``Y``.  Holds
+    references to every buffer the graph reads or writes."""
+
+    def __init__(self, Wgu, Wd, M: int, X=None, out: dict | None = None, ws=None):
+        D = Wd.shape[0]
+        dev, dt = Wgu.device, Wgu.dtype
+        self.X = torch.empty(M, D, dtype=dt, device=dev) if X is None else X
+        M, D, H = _dims(self.X, Wgu, Wd)
+        out = out or {}
+        self.Y = out.get("Y")
+        self.Y = torch.empty(M, D, dtype=dt, device=dev) if self.Y is None else self.Y
+        self.A = out.get("A")
+        self.A = torch.empty(M, H, dtype=dt, device=dev) if self.A is None else self.A
+        self.ws = workspace(M, D, H, dt, SWIGLU_OP_FWD_NOGRAD, dev) if ws is None else ws
+        self.Wgu, self.Wd = Wgu, Wd
+        torch.cuda.synchronize(dev)  # the workspace's zero-fill is complete before any replay
+        h = ctypes.c_void_p(0)
+        L = lib()
+        with torch.cuda.device(dev):
+            _check(L.swiglu_mlp_graph_create_fwd_nograd(
+                _ptr(self.X), _ptr(Wgu), _ptr(Wd), _ptr(self.Y), _ptr(self.A), M, D, H,
+                dtype_code(dt), _ptr(self.ws), self.ws.numel(), ctypes.byref(h)),
+                "swiglu_mlp_graph_create_fwd_nograd")
+        self._h = h
+        self._L = L
+
+    def launch(self, stream=None):
+        s = torch.cuda.current_stream(self.X.device) if stream is None else stream
+        _check(self._L.swiglu_mlp_graph_launch(self._h, ctypes.c_void_p(s.cuda_stream)),
+               "swiglu_mlp_graph_launch")
+
+    def __call__(self, x=None):
+        if x is not None and x.data_ptr() != self.X.data_ptr():
+            self.X.copy_(x)
+        self.launch()
+        return self.Y
+
+    def close(self):
+        """Destroys the graph after pending launches on this device finish
+        (so the buffers it holds may be freed afterwards)."""
+        if getattr(self, "_h", None) is not None and self._h.value:
+            torch.cuda.synchronize(self.X.device)
+            _check(self._L.swiglu_mlp_graph_destroy(self._h), "swiglu_mlp_graph_destroy")
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def swiglu_mlp_bwd(dY, X, Wgu, Wd, saved, out: dict | None = None, ws=None):
     """Backward: returns (dX [M,D], dWgu [2H,D], dWd [D,H]).  Overwrites the
     G/U columns of ``saved`` with dG/dU (a second call on it is undefined)."""
@@ -227,6 +292,12 @@ def swiglu_mlp_set_cta_pairs(mode: int = 1) -> int:
     """Tensor-core GEMMs on SM pairs: 1 = by size (default), 2 = always,
     0 = never; returns the previous mode."""
     return int(lib().swiglu_mlp_set_cta_pairs(int(mode)))
+
+
+def swiglu_mlp_set_nograd_fused(on: bool = True) -> int:
+    """Few-token no-grad calls as one fused kernel (True) or two kernels;
+    returns the previous setting."""
+    return int(lib().swiglu_mlp_set_nograd_fused(1 if on else 0))
 
 
 def swiglu_mlp_profile_enable(on: bool = True) -> None:

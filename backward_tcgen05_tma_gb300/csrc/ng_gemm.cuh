@@ -46,6 +46,7 @@ struct NgArgs {
   int zero_count;   //   kernel's counters (after the dependency wait)
   int clear_err;    // block 0 clears the error word at start (first kernel of a call)
   int dependent;    // launched as a programmatic dependent of the gate/up kernel
+  int ctas;         // CTAs that share the work (the grid, or fewer in a fused phase)
   void* out;        // A [M, ld_out] or Y [M, ld_out]
   int64_t ld_out;
   uint64_t wait_limit_ns;
@@ -126,6 +127,230 @@ __device__ __forceinline__ int epi_bar_and(int v) {
   return r;
 }
 
+// Epilogue building blocks, run by the 128 epilogue threads (warps 2..5;
+// TMEM lane quarter = warp & 3, lane = weight row of the tile).  ``tacc`` is
+// the accumulator's TMEM address (lane 0), ``acce`` the barrier that hands it
+// back to the MMA warp.
+
+// A whole tile's output straight from TMEM.  gate/up: rows 0..63 hold G and
+// rows 64..127 U of the same 64 hidden units, met through ``ustage``.
+template <int NT, bool GATE_UP, bool BF16>
+__device__ __forceinline__ void ng_store_whole(const NgArgs& a, int tile, uint32_t tacc,
+                                               uint32_t acce, float* ustage) {
+  const int row = (threadIdx.x & 96) + (threadIdx.x & 31);  // (warp & 3) * 32 + lane
+  tc_fence_after();
+  const uint32_t taddr = tacc + ((uint32_t)(row & 96) << 16);
+  float v[NT];
+#pragma unroll
+  for (int c = 0; c < NT; c += 16) {
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(taddr + c, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[c + q] = __uint_as_float(r[q]);
+  }
+  tc_fence_before();
+  mbar_arrive(acce);
+  if (GATE_UP) {
+    // rows 64..127 (U) hand their values to rows 0..63 (G) of the same unit
+    if (row >= 64) {
+#pragma unroll
+      for (int n = 0; n < NT; n += 4)
+        *reinterpret_cast<float4*>(ustage + (row - 64) * NT + n) =
+            make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
+    }
+    epi_bar_sync();
+    const int j = tile * 64 + row;
+    if (row < 64 && j < a.rows) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        if (n < a.M) {
+          const float o = silu_f32(v[n]) * ustage[row * NT + n];
+          if (BF16)
+            reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)n * a.ld_out + j] =
+                __float2bfloat16_rn(o);
+          else
+            reinterpret_cast<__half*>(a.out)[(int64_t)n * a.ld_out + j] = __float2half_rn(o);
+        }
+      }
+    }
+    epi_bar_sync();  // ustage is free again
+  } else {
+    const int d = tile * 128 + row;
+    if (d < a.rows) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        if (n < a.M) {
+          if (BF16)
+            reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)n * a.ld_out + d] =
+                __float2bfloat16_rn(v[n]);
+          else
+            reinterpret_cast<__half*>(a.out)[(int64_t)n * a.ld_out + d] = __float2half_rn(v[n]);
+        }
+      }
+    }
+  }
+}
+
+// The accumulator as an fp32 partial tile [128][NT] at ``dst`` (then made
+// visible GPU-wide).
+template <int NT>
+__device__ __forceinline__ void ng_store_partial(float* dst, uint32_t tacc, uint32_t acce) {
+  const int row = (threadIdx.x & 96) + (threadIdx.x & 31);
+  tc_fence_after();
+  float* drow = dst + (size_t)row * NT;
+  const uint32_t taddr = tacc + ((uint32_t)(row & 96) << 16);
+#pragma unroll
+  for (int c = 0; c < NT; c += 16) {
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(taddr + c, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      reinterpret_cast<float4*>(drow + c)[q] =
+          make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                      __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+  }
+  tc_fence_before();
+  mbar_arrive(acce);  // accumulator free for the unit after next
+  __threadfence();
+}
+
+// Sums the n partial tiles part_of(0), ..., part_of(n-1) in that order and
+// writes the tile's output (gate/up: A = rnd(SiLU(g) * u); down: Y = rnd(y)).
+template <int NT, bool GATE_UP, bool BF16, class PartOf>
+__device__ __forceinline__ void ng_reduce_store(const NgArgs& a, int tile, int n, PartOf part_of) {
+  // partials loaded per batch (the down tiles' per-thread share is half the
+  // gate/up pair's)
+  constexpr int RB = GATE_UP ? (NT <= 16 ? 4 : (NT <= 32 ? 2 : 1)) : (NT <= 16 ? 8 : (NT <= 32 ? 4 : 2));
+  const int e = threadIdx.x - 64;  // 0..127 among the epilogue threads
+  if (GATE_UP) {
+    // thread e: hidden unit tile*64 + (e & 63), tokens [h*NT/2, (h+1)*NT/2)
+    const int jr = e & 63, h = e >> 6;
+    const int j = tile * 64 + jr;
+    float g[NT / 2], uu[NT / 2];
+#pragma unroll
+    for (int q = 0; q < NT / 2; ++q) g[q] = uu[q] = 0.0f;
+    for (int i0 = 0; i0 < n; i0 += RB) {
+      // issue the loads of up to RB partials, then add them in order
+      float4 vg[RB][NT / 8], vu[RB][NT / 8];
+#pragma unroll
+      for (int q = 0; q < RB; ++q)
+        if (i0 + q < n) {
+          const float* pb = part_of(i0 + q);
+#pragma unroll
+          for (int k = 0; k < NT / 8; ++k) {
+            vg[q][k] = __ldcg(reinterpret_cast<const float4*>(pb + jr * NT + h * (NT / 2)) + k);
+            vu[q][k] = __ldcg(reinterpret_cast<const float4*>(pb + (64 + jr) * NT + h * (NT / 2)) + k);
+          }
+        }
+#pragma unroll
+      for (int q = 0; q < RB; ++q)
+        if (i0 + q < n) {
+#pragma unroll
+          for (int k = 0; k < NT / 8; ++k) {
+            g[4 * k] += vg[q][k].x; g[4 * k + 1] += vg[q][k].y;
+            g[4 * k + 2] += vg[q][k].z; g[4 * k + 3] += vg[q][k].w;
+            uu[4 * k] += vu[q][k].x; uu[4 * k + 1] += vu[q][k].y;
+            uu[4 * k + 2] += vu[q][k].z; uu[4 * k + 3] += vu[q][k].w;
+          }
+        }
+    }
+    if (j < a.rows) {
+#pragma unroll
+      for (int q = 0; q < NT / 2; ++q) {
+        const int m = h * (NT / 2) + q;
+        if (m < a.M) {
+          const float v = silu_f32(g[q]) * uu[q];
+          if (BF16)
+            reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)m * a.ld_out + j] =
+                __float2bfloat16_rn(v);
+          else
+            reinterpret_cast<__half*>(a.out)[(int64_t)m * a.ld_out + j] = __float2half_rn(v);
+        }
+      }
+    }
+  } else {
+    // thread e: output feature tile*128 + e, all tokens
+    const int d = tile * 128 + e;
+    float y[NT];
+#pragma unroll
+    for (int q = 0; q < NT; ++q) y[q] = 0.0f;
+    for (int i0 = 0; i0 < n; i0 += RB) {
+      float4 v[RB][NT / 4];
+#pragma unroll
+      for (int q = 0; q < RB; ++q)
+        if (i0 + q < n) {
+          const float* pb = part_of(i0 + q) + e * NT;
+#pragma unroll
+          for (int k = 0; k < NT / 4; ++k) v[q][k] = __ldcg(reinterpret_cast<const float4*>(pb) + k);
+        }
+#pragma unroll
+      for (int q = 0; q < RB; ++q)
+        if (i0 + q < n) {
+#pragma unroll
+          for (int k = 0; k < NT / 4; ++k) {
+            y[4 * k] += v[q][k].x; y[4 * k + 1] += v[q][k].y;
+            y[4 * k + 2] += v[q][k].z; y[4 * k + 3] += v[q][k].w;
+          }
+        }
+    }
+    if (d < a.rows) {
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        if (q < a.M) {
+          if (BF16)
+            reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)q * a.ld_out + d] =
+                __float2bfloat16_rn(y[q]);
+          else
+            reinterpret_cast<__half*>(a.out)[(int64_t)q * a.ld_out + d] = __float2half_rn(y[q]);
+        }
+      }
+    }
+  }
+}
+
+// One segment's epilogue in the stream-K split: a whole tile's output from
+// TMEM; else this CTA's partial to the workspace, and the tile's last
+// contributor (per-tile arrival counter) sums the partials in CTA order and
+// writes the output.  Returns true when this CTA wrote the tile's output.
+template <int NT, bool GATE_UP, bool BF16>
+__device__ __forceinline__ bool ng_epilogue_segment(const NgArgs& a, int tile, bool whole, int seg,
+                                                    uint32_t tacc, uint32_t acce, int64_t total,
+                                                    int64_t ctas, float* ustage,
+                                                    volatile int* abort_flag,
+                                                    volatile int* last_flag) {
+  if (whole) {
+    ng_store_whole<NT, GATE_UP, BF16>(a, tile, tacc, acce, ustage);
+    return true;
+  }
+  ng_store_partial<NT>(a.part + ((size_t)blockIdx.x * a.seg_max + seg) * 128 * NT, tacc, acce);
+  // CTAs sharing this tile: owners of its first and last k-block
+  const int c_first = ng_owner((int64_t)tile * a.kb_tile, total, ctas);
+  const int c_last = ng_owner((int64_t)(tile + 1) * a.kb_tile - 1, total, ctas);
+  const int nparts = c_last - c_first + 1;
+  const int e = threadIdx.x - 64;
+  epi_bar_sync();
+  if (e == 0) {
+    int last = 0;
+    if (!*abort_flag) last = atomicAdd(a.counters + tile, 1) == nparts - 1;
+    *last_flag = last;
+  }
+  epi_bar_sync();
+  const int last = *last_flag;
+  if (last) {
+    __threadfence();
+    // partial of CTA c for this tile: its segment index is tile - (first tile of c)
+    ng_reduce_store<NT, GATE_UP, BF16>(a, tile, nparts, [&](int i) -> const float* {
+      const int c = c_first + i;
+      const int j = tile - (int)(ng_start(c, total, ctas) / a.kb_tile);
+      return a.part + ((size_t)c * a.seg_max + j) * 128 * NT;
+    });
+    if (e == 0) a.counters[tile] = 0;  // ready for the next call
+  }
+  return last != 0;
+}
+
 constexpr int NG_THREADS = 192;  // producer warp, MMA warp, 4 epilogue warps
 
 template <int NT, bool GATE_UP, bool BF16>
@@ -136,9 +361,6 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
   static_assert(NT == 16 || NT == 32 || NT == 64, "NT must be 16, 32 or 64");
   static_assert(L::TOTAL + 1024 <= 232448, "shared memory plan exceeds 227 KB");
   constexpr int TILE_ROWS = GATE_UP ? 64 : 128;  // output rows (hidden units / features) per tile
-  // partials loaded per reduction batch (the down kernel's tiles have more
-  // contributors; its per-thread partial is half the gate/up one's pair)
-  constexpr int RB = GATE_UP ? (NT <= 16 ? 4 : (NT <= 32 ? 2 : 1)) : (NT <= 16 ? 8 : (NT <= 32 ? 4 : 2));
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -326,9 +548,6 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // weight row of the tile = TMEM lane
-    const int e = threadIdx.x - 64;       // 0..127 among the epilogue threads
     int acc = 0;
     uint32_t acc_phase = 0;
     int seg = 0;
@@ -342,192 +561,9 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
         ok = mbar_wait_bounded(accf_bar(acc), acc_phase, a.wait_limit_ns, abort_flag, a.err) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!epi_bar_and(ok)) break;  // all four epilogue warps leave together
-      if (whole) {
-        // whole tile: the output straight from TMEM
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * NT;
-        float v[NT];
-#pragma unroll
-        for (int c = 0; c < NT; c += 16) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(taddr + c, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q = 0; q < 16; ++q) v[c + q] = __uint_as_float(r[q]);
-        }
-        tc_fence_before();
-        mbar_arrive(acce_bar(acc));
-        if (GATE_UP) {
-          // rows 64..127 (U) hand their values to rows 0..63 (G) of the same unit
-          if (row >= 64) {
-#pragma unroll
-            for (int n = 0; n < NT; n += 4)
-              *reinterpret_cast<float4*>(ustage + (row - 64) * NT + n) =
-                  make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
-          }
-          epi_bar_sync();
-          const int j = tile * 64 + row;
-          if (row < 64 && j < a.rows) {
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-              if (n < a.M) {
-                const float o = silu_f32(v[n]) * ustage[row * NT + n];
-                if (BF16)
-                  reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)n * a.ld_out + j] =
-                      __float2bfloat16_rn(o);
-                else
-                  reinterpret_cast<__half*>(a.out)[(int64_t)n * a.ld_out + j] = __float2half_rn(o);
-              }
-            }
-          }
-          epi_bar_sync();  // ustage is free again
-        } else {
-          const int d = tile * 128 + row;
-          if (d < a.rows) {
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-              if (n < a.M) {
-                if (BF16)
-                  reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)n * a.ld_out + d] =
-                      __float2bfloat16_rn(v[n]);
-                else
-                  reinterpret_cast<__half*>(a.out)[(int64_t)n * a.ld_out + d] =
-                      __float2half_rn(v[n]);
-              }
-            }
-          }
-        }
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
-        continue;
-      }
-      {
-        tc_fence_after();
-        float* dst = a.part + (((size_t)blockIdx.x * a.seg_max + seg) * 128 + row) * NT;
-        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * NT;
-#pragma unroll
-        for (int c = 0; c < NT; c += 16) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(taddr + c, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            reinterpret_cast<float4*>(dst + c)[q] =
-                make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                            __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-        }
-        tc_fence_before();
-        mbar_arrive(acce_bar(acc));  // accumulator free for the unit after next
-        __threadfence();
-      }
-      // CTAs sharing this tile: owners of its first and last k-block
-      const int c_first = ng_owner((int64_t)tile * a.kb_tile, total, ctas);
-      const int c_last = ng_owner((int64_t)(tile + 1) * a.kb_tile - 1, total, ctas);
-      const int nparts = c_last - c_first + 1;
-      epi_bar_sync();
-      if (e == 0) {
-        int last = 0;
-        if (!*abort_flag) last = atomicAdd(a.counters + tile, 1) == nparts - 1;
-        *last_flag = last;
-      }
-      epi_bar_sync();
-      const int last = *last_flag;
-      if (last) {
-        __threadfence();
-        // partial of CTA c for this tile: its segment index is tile - (first tile of c)
-        auto part_of = [&](int c) -> const float* {
-          const int j = tile - (int)(ng_start(c, total, ctas) / a.kb_tile);
-          return a.part + ((size_t)c * a.seg_max + j) * 128 * NT;
-        };
-        if (GATE_UP) {
-          // thread e: hidden unit tile*64 + (e & 63), tokens [h*NT/2, (h+1)*NT/2)
-          const int jr = e & 63, h = e >> 6;
-          const int j = tile * 64 + jr;
-          float g[NT / 2], uu[NT / 2];
-#pragma unroll
-          for (int n = 0; n < NT / 2; ++n) g[n] = uu[n] = 0.0f;
-          for (int c0 = c_first; c0 <= c_last; c0 += RB) {
-            // issue the loads of up to RB partials, then add them in CTA order
-            float4 vg[RB][NT / 8], vu[RB][NT / 8];
-#pragma unroll
-            for (int q = 0; q < RB; ++q)
-              if (c0 + q <= c_last) {
-                const float* pb = part_of(c0 + q);
-#pragma unroll
-                for (int n = 0; n < NT / 8; ++n) {
-                  vg[q][n] = __ldcg(reinterpret_cast<const float4*>(pb + jr * NT + h * (NT / 2)) + n);
-                  vu[q][n] = __ldcg(reinterpret_cast<const float4*>(pb + (64 + jr) * NT + h * (NT / 2)) + n);
-                }
-              }
-#pragma unroll
-            for (int q = 0; q < RB; ++q)
-              if (c0 + q <= c_last) {
-#pragma unroll
-                for (int n = 0; n < NT / 8; ++n) {
-                  g[4 * n] += vg[q][n].x; g[4 * n + 1] += vg[q][n].y;
-                  g[4 * n + 2] += vg[q][n].z; g[4 * n + 3] += vg[q][n].w;
-                  uu[4 * n] += vu[q][n].x; uu[4 * n + 1] += vu[q][n].y;
-                  uu[4 * n + 2] += vu[q][n].z; uu[4 * n + 3] += vu[q][n].w;
-                }
-              }
-          }
-          if (j < a.rows) {
-#pragma unroll
-            for (int n = 0; n < NT / 2; ++n) {
-              const int m = h * (NT / 2) + n;
-              if (m < a.M) {
-                const float v = silu_f32(g[n]) * uu[n];
-                if (BF16)
-                  reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)m * a.ld_out + j] =
-                      __float2bfloat16_rn(v);
-                else
-                  reinterpret_cast<__half*>(a.out)[(int64_t)m * a.ld_out + j] = __float2half_rn(v);
-              }
-            }
-          }
-        } else {
-          // thread e: output feature tile*128 + e, all tokens
-          const int d = tile * 128 + e;
-          float y[NT];
-#pragma unroll
-          for (int n = 0; n < NT; ++n) y[n] = 0.0f;
-          for (int c0 = c_first; c0 <= c_last; c0 += RB) {
-            float4 v[RB][NT / 4];
-#pragma unroll
-            for (int q = 0; q < RB; ++q)
-              if (c0 + q <= c_last) {
-                const float* pb = part_of(c0 + q) + e * NT;
-#pragma unroll
-                for (int n = 0; n < NT / 4; ++n) v[q][n] = __ldcg(reinterpret_cast<const float4*>(pb) + n);
-              }
-#pragma unroll
-            for (int q = 0; q < RB; ++q)
-              if (c0 + q <= c_last) {
-#pragma unroll
-                for (int n = 0; n < NT / 4; ++n) {
-                  y[4 * n] += v[q][n].x; y[4 * n + 1] += v[q][n].y;
-                  y[4 * n + 2] += v[q][n].z; y[4 * n + 3] += v[q][n].w;
-                }
-              }
-          }
-          if (d < a.rows) {
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-              if (n < a.M) {
-                if (BF16)
-                  reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)n * a.ld_out + d] =
-                      __float2bfloat16_rn(y[n]);
-                else
-                  reinterpret_cast<__half*>(a.out)[(int64_t)n * a.ld_out + d] =
-                      __float2half_rn(y[n]);
-              }
-            }
-          }
-        }
-        if (e == 0) a.counters[tile] = 0;  // ready for the next call
-      }
+      ng_epilogue_segment<NT, GATE_UP, BF16>(a, tile, whole, seg, tmem_base + acc * NT,
+                                             acce_bar(acc), total, ctas, ustage, abort_flag,
+                                             last_flag);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;

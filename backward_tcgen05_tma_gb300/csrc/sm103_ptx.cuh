@@ -102,6 +102,40 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
+// Non-blocking test of a phase: never suspends the thread, so a loop can poll
+// other conditions between tests.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// ---------------------------------------------------------------------------
+// flags in global memory passed between the CTAs of one grid (gpu scope)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_or_release_gpu(uint32_t* p, uint32_t bits) {
+  asm volatile("red.release.gpu.global.or.b32 [%0], %1;" ::"l"(p), "r"(bits) : "memory");
+}
+
+// Orders this thread's generic-proxy accesses to global memory with its
+// async-proxy ones (TMA): a writer issues it after storing data that another
+// CTA's TMA will read, a reader after acquiring the flag and before the TMA.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // programmatic dependent launch
 // ---------------------------------------------------------------------------

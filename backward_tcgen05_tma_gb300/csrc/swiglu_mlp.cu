@@ -20,6 +20,7 @@
 #include <vector>
 
 #include "../../include/swiglu_mlp.h"
+#include "ng_fused.cuh"
 #include "ng_gemm.cuh"
 #include "simt_gemm.cuh"
 #include "tc2_gemm.cuh"
@@ -39,6 +40,7 @@ swiglu_status cuda_status(cudaError_t e);
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_last_launches{0};
 std::atomic<int> g_cta_pairs{1};  // SM pairs (cta_group::2): 0 never, 1 by size, 2 always
+std::atomic<int> g_ng_fused{0};   // few-token no-grad: 1 one fused kernel, 0 two kernels
 constexpr int TC2_STAGES = 6;
 
 // ---------------------------------------------------------------------------
@@ -47,12 +49,12 @@ constexpr int TC2_STAGES = 6;
 enum KernelId : int {
   K_GATE_UP = 0, K_DOWN, K_DGU, K_DWD, K_DWGU, K_DX, K_GATE_UP_NOGRAD, K_DOWN_NOGRAD,
   K_SIMT_GATE_UP, K_SIMT_DOWN, K_SIMT_DGU, K_SIMT_DWD, K_SIMT_DWGU, K_SIMT_DX, K_NG_GATE_UP,
-  K_NG_DOWN, K_COUNT
+  K_NG_DOWN, K_NG_FUSED, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
     "gate_up_swiglu", "down_proj", "dgu_inplace", "dwd", "dwgu", "dx", "gate_up_nograd",
     "down_proj_nograd", "simt_gate_up_swiglu", "simt_down_proj", "simt_dgu_inplace", "simt_dwd",
-    "simt_dwgu", "simt_dx", "nograd_small_gate_up", "nograd_small_down"};
+    "simt_dwgu", "simt_dx", "nograd_small_gate_up", "nograd_small_down", "nograd_small_fused"};
 
 struct ProfRec {
   int id;
@@ -400,24 +402,70 @@ NgPlan ng_plan(int64_t M, int64_t D, int64_t H) {
   p.kb1 = (int)((D + 63) / 64);
   p.t2 = (int)((D + 127) / 128);
   p.kb2 = (int)((H + 63) / 64);
-  p.counter_bytes = (((size_t)(p.t1 + p.t2) * 4 + 255) / 256) * 256;
+  // arrival counters of both phases, then the fused kernel's ready mask
+  p.counter_bytes = (((size_t)(p.t1 + p.t2 + (p.t1 + 31) / 32) * 4 + 255) / 256) * 256;
   const size_t slots = (size_t)(p.t1 > p.t2 ? p.t1 : p.t2) + 3 * NG_MAX_CTAS;
   p.part_bytes = slots * 128 * p.NT * 4;
   return p;
 }
 
-// Grid, stream-K tiles and partial slots per CTA.  With tiles >= CTAs, all
-// but (tiles mod CTAs) tiles are taken whole, the same number per CTA.
-void ng_grid(int tiles, int kb, int& ctas, int& sk_tiles, int& seg_max) {
-  int nsm = sm_count();
-  if (nsm < 1) nsm = 1;
-  int64_t c = nsm < NG_MAX_CTAS ? nsm : NG_MAX_CTAS;
+// CTAs, stream-K tiles and partial slots per CTA of one GEMM over at most
+// `grid` CTAs.  With tiles >= CTAs, all but (tiles mod CTAs) tiles are taken
+// whole, the same number per CTA; with fewer k-blocks than CTAs to share, the
+// count shrinks so that every sharing CTA owns at least one.
+void ng_split(int tiles, int kb, int grid, int& ctas, int& sk_tiles, int& seg_max) {
+  int64_t c = grid < 1 ? 1 : grid;
   sk_tiles = tiles >= c ? (int)(tiles % c) : tiles;
   const int64_t total = (int64_t)sk_tiles * kb;
   if (total > 0 && c > total && tiles < c) c = total;
   ctas = (int)c;
   const int64_t range = total > 0 ? (total + c - 1) / c : 0;
   seg_max = (int)((range + kb - 1) / kb) + 1;
+}
+
+int ng_max_grid() {
+  const int nsm = sm_count();
+  return nsm < 1 ? 1 : (nsm < NG_MAX_CTAS ? nsm : NG_MAX_CTAS);
+}
+
+void ng_grid(int tiles, int kb, int& ctas, int& sk_tiles, int& seg_max) {
+  ng_split(tiles, kb, ng_max_grid(), ctas, sk_tiles, seg_max);
+}
+
+// The fused kernel's one grid and each phase's split of it.
+struct NgFusedPlan {
+  int grid;
+  int c0, sk0, seg0;  // gate/up
+  int c1, sk1, seg1;  // down
+  size_t part0_bytes, part1_bytes;
+};
+
+NgFusedPlan ng_fused_plan(const NgPlan& p) {
+  NgFusedPlan f;
+  const int g = ng_max_grid();
+  ng_split(p.t1, p.kb1, g, f.c0, f.sk0, f.seg0);
+  ng_split(p.t2, p.kb2, g, f.c1, f.sk1, f.seg1);
+  f.grid = f.c0 > f.c1 ? f.c0 : f.c1;
+  f.part0_bytes = (size_t)f.c0 * f.seg0 * 128 * p.NT * 4;
+  f.part1_bytes = (size_t)f.c1 * f.seg1 * 128 * p.NT * 4;
+  return f;
+}
+
+// Workspace bytes of the fused kernel on the current device: both phases'
+// partial tiles are live at once.
+size_t ng_fused_bytes(const NgPlan& p) {
+  const NgFusedPlan f = ng_fused_plan(p);
+  return WS_HEADER + p.counter_bytes + f.part0_bytes + f.part1_bytes;
+}
+
+// Workspace bytes of the two-kernel form with the current device's grids
+// (the second kernel reuses the first one's partial slots).
+size_t ng_two_bytes(const NgPlan& p) {
+  int c1 = 1, s1 = 1, c2 = 1, s2 = 1, k1 = 0, k2 = 0;
+  ng_grid(p.t1, p.kb1, c1, k1, s1);
+  ng_grid(p.t2, p.kb2, c2, k2, s2);
+  const size_t slots1 = (size_t)c1 * s1, slots2 = (size_t)c2 * s2;
+  return WS_HEADER + p.counter_bytes + (slots1 > slots2 ? slots1 : slots2) * 128 * p.NT * 4;
 }
 
 template <int NT, bool GATE_UP, bool BF16>
@@ -429,6 +477,7 @@ cudaError_t launch_ng(int kid, const CUtensorMap& tw, const CUtensorMap& tx, NgA
   if (e != cudaSuccess) return e;
   int grid = 1;
   ng_grid(a.tiles, a.kb_tile, grid, a.sk_tiles, a.seg_max);
+  a.ctas = grid;
   ProfScope prof(kid, st);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -466,25 +515,109 @@ swiglu_status ng_forward_nt(const void* X, const void* Wgu, const void* Wd, void
   CUtensorMap tw, tx;
   if (!encode_gateup(&tw, BF16, Wgu, D, H, 64) || !map_kmajor(&tx, BF16, X, D, M, D, NT))
     return SWIGLU_ERR_CUDA;
-  NgArgs a1{(int)M, (int)H, p.kb1, p.t1, 0, 0, part, counters, counters + p.t1, p.t2, 1, 0,
+  NgArgs a1{(int)M, (int)H, p.kb1, p.t1, 0, 0, part, counters, counters + p.t1, p.t2, 1, 0, 0,
             A, H, wl, err};
   if (launch_ng<NT, true, BF16>(K_NG_GATE_UP, tw, tx, a1, st) != cudaSuccess)
     return SWIGLU_ERR_CUDA;
   if (!map_kmajor(&tw, BF16, Wd, H, D, H, 128) || !map_kmajor(&tx, BF16, A, H, M, H, NT))
     return SWIGLU_ERR_CUDA;
-  NgArgs a2{(int)M, (int)D, p.kb2, p.t2, 0, 0, part, counters + p.t1, counters, p.t1, 0, 1,
+  NgArgs a2{(int)M, (int)D, p.kb2, p.t2, 0, 0, part, counters + p.t1, counters, p.t1, 0, 1, 0,
             Y, D, wl, err};
   return cuda_status(launch_ng<NT, false, BF16>(K_NG_DOWN, tw, tx, a2, st));
 }
 
+constexpr size_t NG_DONE_OFFSET = 128;  // the fused kernel's finished-CTA count (header)
+
+// Whether the fused kernel's grid can be resident all at once on the current
+// device (queried once per device).
+template <int NT, bool BF16>
+bool ng_fused_fits(int grid) {
+  static std::mutex mu;
+  static int cached[64];  // 0 unknown, else 1 + blocks per SM
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> g(mu);
+  if (cached[dev] == 0) {
+    auto kern = ng_fused_kernel<NT, BF16>;
+    constexpr int smem = NgSmem<NT>::DYN_BYTES;
+    int nb = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, NG_THREADS, smem) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      nb = 0;
+    }
+    cached[dev] = 1 + nb;
+  }
+  return (int64_t)(cached[dev] - 1) * sm_count() >= grid;
+}
+
+// The fused form: one cooperative launch for both GEMMs.  ws layout as for
+// the two kernels, plus the ready mask after the counters, the finished-CTA
+// count in the header, and the two phases' partial tiles side by side.
+template <int NT, bool BF16>
+swiglu_status ng_forward_fused(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
+                               int64_t M, int64_t D, int64_t H, const NgPlan& p, char* ws,
+                               cudaStream_t st) {
+  const NgFusedPlan fp = ng_fused_plan(p);
+  int* err = reinterpret_cast<int*>(ws);
+  int* counters = reinterpret_cast<int*>(ws + WS_HEADER);
+  NgFusedArgs f;
+  f.ready = reinterpret_cast<uint32_t*>(counters + p.t1 + p.t2);
+  f.done = reinterpret_cast<uint32_t*>(ws + NG_DONE_OFFSET);
+  f.inject_unready = g_inject_stall.exchange(0);
+  float* part0 = reinterpret_cast<float*>(ws + WS_HEADER + p.counter_bytes);
+  float* part1 = reinterpret_cast<float*>(ws + WS_HEADER + p.counter_bytes + fp.part0_bytes);
+  const uint64_t wl = g_wait_limit_ns.load();
+  CUtensorMap twgu, tx, twd, ta;
+  if (!encode_gateup(&twgu, BF16, Wgu, D, H, 64) || !map_kmajor(&tx, BF16, X, D, M, D, NT) ||
+      !map_kmajor(&twd, BF16, Wd, H, D, H, 128) || !map_kmajor(&ta, BF16, A, H, M, H, NT))
+    return SWIGLU_ERR_CUDA;
+  f.ph[0] = NgArgs{(int)M, (int)H, p.kb1, p.t1, fp.sk0, fp.seg0, part0, counters, nullptr, 0, 1,
+                   0, fp.c0, A, H, wl, err};
+  f.ph[1] = NgArgs{(int)M, (int)D, p.kb2, p.t2, fp.sk1, fp.seg1, part1, counters + p.t1, nullptr,
+                   0, 0, 0, fp.c1, Y, D, wl, err};
+  auto kern = ng_fused_kernel<NT, BF16>;
+  ProfScope prof(K_NG_FUSED, st);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)fp.grid);
+  cfg.blockDim = dim3(NG_THREADS);
+  cfg.dynamicSmemBytes = NgSmem<NT>::DYN_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // phase 1 waits on flags other CTAs raise
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, twgu, tx, twd, ta, f);
+  g_last_launches.fetch_add(1);
+  if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
+  return cuda_status(cudaGetLastError());
+}
+
+// The fused form when it is enabled and its grid fits the device (and,
+// for a fixed scratch array, its workspace fits `ws_cap`), else two kernels.
+template <int NT, bool BF16>
+swiglu_status ng_forward_t(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
+                           int64_t M, int64_t D, int64_t H, const NgPlan& p, char* ws,
+                           size_t ws_cap, cudaStream_t st) {
+  if (g_ng_fused.load() != 0 && ng_fused_bytes(p) <= ws_cap &&
+      ng_fused_fits<NT, BF16>(ng_fused_plan(p).grid))
+    return ng_forward_fused<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, st);
+  if (ng_two_bytes(p) > ws_cap) return SWIGLU_ERR_UNSUPPORTED;
+  return ng_forward_nt<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, st);
+}
+
 template <bool BF16>
 swiglu_status ng_forward(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
-                         int64_t M, int64_t D, int64_t H, char* ws, cudaStream_t st) {
+                         int64_t M, int64_t D, int64_t H, char* ws, size_t ws_cap,
+                         cudaStream_t st) {
   const NgPlan p = ng_plan(M, D, H);
   switch (p.NT) {
-    case 16: return ng_forward_nt<16, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, st);
-    case 32: return ng_forward_nt<32, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, st);
-    default: return ng_forward_nt<64, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, st);
+    case 16: return ng_forward_t<16, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, st);
+    case 32: return ng_forward_t<32, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, st);
+    default: return ng_forward_t<64, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, st);
   }
 }
 
@@ -494,7 +627,7 @@ swiglu_status ng_forward(const void* X, const void* Wgu, const void* Wd, void* Y
 // Scratch (error word, tile counters, fp32 partial tiles) for callers that
 // cannot allocate.  It is part of the module image: every GPU that loads this
 // library holds these bytes until the process exits.
-constexpr size_t NOALLOC_SCRATCH_BYTES = 8u << 20;
+constexpr size_t NOALLOC_SCRATCH_BYTES = 16u << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
 constexpr int NOALLOC_MAX_DEVICES = 64;
@@ -517,15 +650,6 @@ swiglu_status noalloc_scratch(void** out) {
   }
   *out = g_noalloc_ptr[dev];
   return SWIGLU_OK;
-}
-
-// Scratch bytes one call needs on the current device (its actual grids).
-size_t noalloc_bytes_needed(const NgPlan& p) {
-  int c1 = 1, s1 = 1, c2 = 1, s2 = 1, k1 = 0, k2 = 0;
-  ng_grid(p.t1, p.kb1, c1, k1, s1);
-  ng_grid(p.t2, p.kb2, c2, k2, s2);
-  const size_t slots1 = (size_t)c1 * s1, slots2 = (size_t)c2 * s2;
-  return WS_HEADER + p.counter_bytes + (slots1 > slots2 ? slots1 : slots2) * 128 * p.NT * 4;
 }
 
 size_t elt_bytes(swiglu_dtype dt) {
@@ -708,7 +832,9 @@ size_t swiglu_mlp_saved_bytes(int64_t M, int64_t H, swiglu_dtype dtype) {
 size_t swiglu_mlp_workspace_bytes(int64_t M, int64_t D, int64_t H, swiglu_dtype dtype, int op) {
   if (op == SWIGLU_OP_FWD_NOGRAD && D > 0 && H > 0 && ng_eligible(M, D, H, dtype)) {
     const NgPlan p = ng_plan(M, D, H);
-    return WS_HEADER + p.counter_bytes + p.part_bytes;
+    const size_t two = WS_HEADER + p.counter_bytes + p.part_bytes;
+    const size_t one = ng_fused_bytes(p);
+    return two > one ? two : one;
   }
   if (dtype == SWIGLU_BF16 || dtype == SWIGLU_F16)
     return WS_HEADER + TC_SK_COUNTER_BYTES + tc_ws_part_bytes(M, D, H, op);
@@ -753,8 +879,8 @@ swiglu_status swiglu_mlp_fwd_nograd(const void* X, const void* Wgu, const void* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (ng_eligible(M, D, H, dtype)) {
     char* w = static_cast<char*>(ws);
-    return dtype == SWIGLU_BF16 ? ng_forward<true>(X, Wgu, Wd, Y, A, M, D, H, w, s)
-                                : ng_forward<false>(X, Wgu, Wd, Y, A, M, D, H, w, s);
+    return dtype == SWIGLU_BF16 ? ng_forward<true>(X, Wgu, Wd, Y, A, M, D, H, w, ws_bytes, s)
+                                : ng_forward<false>(X, Wgu, Wd, Y, A, M, D, H, w, ws_bytes, s);
   }
   int* err = static_cast<int*>(ws);
   if (cudaMemsetAsync(err, 0, ws_clear_bytes(dtype), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
@@ -783,15 +909,18 @@ swiglu_status swiglu_mlp_fwd_nograd_noalloc(const void* X, const void* Wgu, cons
   void* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != SWIGLU_OK) return st;
   const NgPlan p = ng_plan(M, D, H);
-  if (noalloc_bytes_needed(p) > NOALLOC_SCRATCH_BYTES) return SWIGLU_ERR_UNSUPPORTED;
+  if (ng_two_bytes(p) > NOALLOC_SCRATCH_BYTES &&
+      (g_ng_fused.load() == 0 || ng_fused_bytes(p) > NOALLOC_SCRATCH_BYTES))
+    return SWIGLU_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the array keeps the previous call's contents: clear the error word and
-  // the tile counters, which must start at zero
+  // the array keeps the previous call's contents: clear the error word, the
+  // tile counters and the ready mask, which must start at zero
   if (cudaMemsetAsync(scratch, 0, WS_HEADER + p.counter_bytes, s) != cudaSuccess)
     return SWIGLU_ERR_CUDA;
   char* w = static_cast<char*>(scratch);
-  return dtype == SWIGLU_BF16 ? ng_forward<true>(X, Wgu, Wd, Y, A, M, D, H, w, s)
-                              : ng_forward<false>(X, Wgu, Wd, Y, A, M, D, H, w, s);
+  return dtype == SWIGLU_BF16
+             ? ng_forward<true>(X, Wgu, Wd, Y, A, M, D, H, w, NOALLOC_SCRATCH_BYTES, s)
+             : ng_forward<false>(X, Wgu, Wd, Y, A, M, D, H, w, NOALLOC_SCRATCH_BYTES, s);
 }
 
 swiglu_status swiglu_mlp_bwd(const void* dY, const void* X, const void* Wgu, const void* Wd,
@@ -816,6 +945,83 @@ swiglu_status swiglu_mlp_bwd(const void* dY, const void* X, const void* Wgu, con
                            (const float*)Wd, (float*)saved, (float*)dX, (float*)dWgu,
                            (float*)dWd, M, D, H, s);
   }
+}
+
+struct swiglu_mlp_graph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int device = -1;
+  int launches = 0;  // kernels one replay runs
+};
+
+swiglu_status swiglu_mlp_graph_create_fwd_nograd(const void* X, const void* Wgu, const void* Wd,
+                                                 void* Y, void* A, int64_t M, int64_t D,
+                                                 int64_t H, swiglu_dtype dtype, void* ws,
+                                                 size_t ws_bytes, swiglu_mlp_graph** out) {
+  if (out == nullptr) return SWIGLU_ERR_INVALID_ARG;
+  *out = nullptr;
+  swiglu_status st = check_common(M, D, H, dtype, ws, ws_bytes, SWIGLU_OP_FWD_NOGRAD);
+  if (st != SWIGLU_OK) return st;
+  if (M > 0 && (st = check_ptrs({X, Wgu, Wd, Y, A})) != SWIGLU_OK) return st;
+  if (g_prof_on.load()) return SWIGLU_ERR_UNSUPPORTED;
+  swiglu_mlp_graph* g = new swiglu_mlp_graph;
+  if (cudaGetDevice(&g->device) != cudaSuccess) {
+    delete g;
+    return SWIGLU_ERR_CUDA;
+  }
+  if (M == 0) {  // nothing to record: launches of this graph do nothing
+    *out = g;
+    return SWIGLU_OK;
+  }
+  // device queries that are cached on first use run here, outside the capture
+  sm_count();
+  if (dtype != SWIGLU_F32_IEEE) tc2_units();
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+    delete g;
+    return SWIGLU_ERR_CUDA;
+  }
+  st = SWIGLU_ERR_CUDA;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+    const swiglu_status inner =
+        swiglu_mlp_fwd_nograd(X, Wgu, Wd, Y, A, M, D, H, dtype, ws, ws_bytes, cs);
+    g->launches = g_last_launches.load();
+    const cudaError_t ec = cudaStreamEndCapture(cs, &g->graph);
+    if (inner != SWIGLU_OK)
+      st = inner;
+    else if (ec == cudaSuccess && g->graph != nullptr &&
+             cudaGraphInstantiate(&g->exec, g->graph, 0) == cudaSuccess)
+      st = SWIGLU_OK;
+  }
+  cudaGetLastError();  // clear the error a failed capture recorded
+  cudaStreamDestroy(cs);
+  if (st != SWIGLU_OK) {
+    swiglu_mlp_graph_destroy(g);
+    return st;
+  }
+  *out = g;
+  return SWIGLU_OK;
+}
+
+swiglu_status swiglu_mlp_graph_launch(swiglu_mlp_graph* graph, void* stream) {
+  if (graph == nullptr) return SWIGLU_ERR_INVALID_ARG;
+  g_last_launches.store(0);
+  if (graph->exec == nullptr) return SWIGLU_OK;  // M = 0
+  const cudaError_t e = cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) g_last_launches.store(graph->launches);
+  return cuda_status(e);
+}
+
+swiglu_status swiglu_mlp_graph_destroy(swiglu_mlp_graph* graph) {
+  if (graph == nullptr) return SWIGLU_ERR_INVALID_ARG;
+  cudaError_t e = cudaSuccess;
+  if (graph->exec != nullptr) e = cudaGraphExecDestroy(graph->exec);
+  if (graph->graph != nullptr) {
+    const cudaError_t e2 = cudaGraphDestroy(graph->graph);
+    if (e == cudaSuccess) e = e2;
+  }
+  delete graph;
+  return cuda_status(e);
 }
 
 swiglu_status swiglu_mlp_query_error(const void* ws, void* stream) {
@@ -850,6 +1056,8 @@ uint64_t swiglu_mlp_set_wait_limit_ns(uint64_t ns) {
 void swiglu_mlp_inject_stall_once(int on) { g_inject_stall.store(on ? 1 : 0); }
 
 int swiglu_mlp_last_launch_count(void) { return g_last_launches.load(); }
+
+int swiglu_mlp_set_nograd_fused(int on) { return g_ng_fused.exchange(on ? 1 : 0); }
 
 int swiglu_mlp_set_cta_pairs(int mode) {
   return g_cta_pairs.exchange(mode <= 0 ? 0 : (mode >= 2 ? 2 : 1));

@@ -377,12 +377,40 @@ def _nograd_sweep(api, device, peaks, sizes=NOGRAD_S):
         kern = {k: round(v[1] / v[0] * 1e3, 2) for k, v in api.swiglu_mlp_profile_read().items()}
         tmed = statistics.median(times)
         byts = metrics.nograd_algorithmic_bytes(S, D, H)
+        loop = _decode_loop(api, X, wts, o, ws)
         res.append({"S": S, "us": round(tmed * 1e6, 2), "GBps": round(byts / tmed / 1e9, 1),
                     "hbm_frac": round(byts / tmed / 1e9 / peaks["hbm_gbs"], 4),
                     "TFLOPS": round(metrics.fwd_flops(S, D, H) / tmed / 1e12, 2),
-                    "kernel_us": kern})
+                    "kernel_us": kern, **loop})
     return {"workload": "B1_D4096_H11008_bf16_nograd", "l2": "flushed (512 MiB read) before "
-            "each timed call", "median_of": 20, "sweep": res}
+            "each timed call", "median_of": 20,
+            "decode_loop": "%d back-to-back calls, host wall clock per call (launch cost "
+                           "included, no flush: the 270 MB of weights exceed L2): direct C-ABI "
+                           "calls vs replays of the captured graph" % DECODE_REPS,
+            "sweep": res}
+
+
+DECODE_REPS = 200
+
+
+def _decode_loop(api, X, wts, o, ws):
+    """Per-call wall time of a decode loop: direct calls vs CUDA-graph replays."""
+    import torch
+    g = api.FwdNogradGraph(wts["Wgu"], wts["Wd"], X.shape[0], X=X, out=o, ws=ws)
+    out = {}
+    for name, call in (("direct", lambda: api.swiglu_mlp_fwd_nograd(X, wts["Wgu"], wts["Wd"],
+                                                                     out=o, ws=ws)),
+                       ("graph", g.launch)):
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(DECODE_REPS):
+            call()
+        torch.cuda.synchronize()
+        out["loop_us_" + name] = round((time.perf_counter() - t0) / DECODE_REPS * 1e6, 2)
+    g.close()
+    return out
 
 
 def _cpu_baseline(t_dev, w):

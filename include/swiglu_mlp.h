@@ -48,7 +48,8 @@
  * remaining tiles are split along K over all SMs (stream-K) and the partial
  * sums meet in the workspace.  After a SWIGLU_ERR_DEVICE_TIMEOUT, zero-fill
  * it again before reuse.  Calls that share one workspace must not overlap on
- * the GPU.  The library itself allocates no memory.
+ * the GPU.  The library itself allocates no device buffers (the one
+ * exception: an instantiated graph of swiglu_mlp_graph_create_fwd_nograd).
  *
  * Calls are asynchronous on ``stream`` and do not synchronise (except
  * swiglu_mlp_query_error).  Argument errors are detected on the host before
@@ -121,14 +122,15 @@ swiglu_status swiglu_mlp_fwd_nograd(const void* X, const void* Wgu, const void* 
  *
  * The caller passes inputs and outputs as in swiglu_mlp_fwd_nograd; there is
  * no workspace argument.  Scratch (error word, per-tile counters, fp32
- * partial sums) lives in one file-scope static device array of 8 MiB, which
+ * partial sums) lives in one file-scope static device array of 16 MiB, which
  * every GPU that loads this library holds until the process exits.  The call
  * allocates nothing (no cudaMalloc/cudaFree, no allocating library routine).
  *
  * Limits: bf16/fp16 only, 0 <= M <= 64, D and H multiples of 8, and the
- * partial sums of the call must fit the array (for D = 4096, H = 11008 on a
- * 152-SM GB300: M <= 32); anything beyond returns SWIGLU_ERR_UNSUPPORTED
- * without launching.
+ * partial sums of the call must fit the array (on a 152-SM GB300 the fused
+ * kernel's fit for M <= 32 and the two-kernel form's for every M <= 64, at
+ * any D and H: each CTA holds at most two partial tiles per GEMM); anything
+ * beyond returns SWIGLU_ERR_UNSUPPORTED without launching.
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
@@ -141,6 +143,41 @@ swiglu_status swiglu_mlp_fwd_nograd(const void* X, const void* Wgu, const void* 
 swiglu_status swiglu_mlp_fwd_nograd_noalloc(const void* X, const void* Wgu, const void* Wd,
                                             void* Y, void* A, int64_t M, int64_t D, int64_t H,
                                             swiglu_dtype dtype, void* stream);
+
+/* A no-grad forward captured once into a CUDA graph and replayed per call,
+ * for decode loops ("Inference results": the fixed host cost of building
+ * descriptors per call dominates at small shapes, and CUDA graphs are the
+ * remedy the page names but did not validate).
+ *
+ * swiglu_mlp_graph_create_fwd_nograd validates its arguments exactly as
+ * swiglu_mlp_fwd_nograd does, then records that call -- its workspace clear,
+ * tensor maps and kernel launches, with every pointer and size fixed -- by
+ * stream capture on a stream of its own, and instantiates the graph for the
+ * current device.  Nothing runs on the GPU during create.  Each
+ * swiglu_mlp_graph_launch(graph, stream) then performs the same computation
+ * on the buffers given at create time: write the new tokens into X, launch,
+ * read Y (and A) after the launch on ``stream`` completes.  Results are
+ * bitwise equal to swiglu_mlp_fwd_nograd on the same inputs.
+ *
+ * Ownership: the caller keeps X, Wgu, Wd, Y, A and ws alive and unmoved for
+ * the life of the graph; ``ws`` follows the workspace rules above (zero-filled
+ * before first use; launches sharing it must not overlap on the GPU).  The
+ * graph object (host memory plus what the CUDA runtime holds for an
+ * instantiated graph) belongs to the library until
+ * swiglu_mlp_graph_destroy(graph); launches still pending then complete, and
+ * the runtime releases the graph after them (the caller's buffers must
+ * outlive those launches).  Create must not itself be called during a stream capture, nor
+ * while per-kernel profiling is enabled (SWIGLU_ERR_UNSUPPORTED).  M = 0
+ * yields a graph whose launch does nothing.  Errors: the argument statuses of
+ * swiglu_mlp_fwd_nograd; SWIGLU_ERR_INVALID_ARG for a NULL ``graph`` /
+ * ``out``; SWIGLU_ERR_CUDA when capture, instantiation or launch fails. */
+typedef struct swiglu_mlp_graph swiglu_mlp_graph;
+swiglu_status swiglu_mlp_graph_create_fwd_nograd(const void* X, const void* Wgu, const void* Wd,
+                                                 void* Y, void* A, int64_t M, int64_t D,
+                                                 int64_t H, swiglu_dtype dtype, void* ws,
+                                                 size_t ws_bytes, swiglu_mlp_graph** out);
+swiglu_status swiglu_mlp_graph_launch(swiglu_mlp_graph* graph, void* stream);
+swiglu_status swiglu_mlp_graph_destroy(swiglu_mlp_graph* graph);
 
 /* Backward.  Consumes ``saved`` as written by swiglu_mlp_fwd on the same
  * X, Wgu, Wd: the expired G/U columns are overwritten in place with dG/dU
@@ -176,9 +213,10 @@ uint64_t swiglu_mlp_set_wait_limit_ns(uint64_t ns);
 
 /* Test hook for failure detection: when ``on`` is nonzero, the next
  * tensor-core launch of this process makes its load producer skip the arrival
- * of the first pipeline stage, so the consumer's wait runs out, the kernel
- * records SWIGLU_ERR_DEVICE_TIMEOUT and returns cleanly.  The flag clears
- * itself after one launch.  Outputs of that call are undefined. */
+ * of the first pipeline stage (or, in the fused few-token no-grad kernel,
+ * leaves the first gate/up tile's ready bit clear), so a consumer's wait runs
+ * out, the kernel records SWIGLU_ERR_DEVICE_TIMEOUT and returns cleanly.  The
+ * flag clears itself after one launch.  Outputs of that call are undefined. */
 void swiglu_mlp_inject_stall_once(int on);
 
 /* Selects how later calls of this process run their bf16/fp16 tensor-core
@@ -191,6 +229,18 @@ void swiglu_mlp_inject_stall_once(int on);
  * the previous mode.  A workspace sized by swiglu_mlp_workspace_bytes() fits
  * every mode. */
 int swiglu_mlp_set_cta_pairs(int mode);
+
+/* Selects how later few-token no-grad calls (M <= 64, bf16/fp16) of this
+ * process run: on = 1 as ONE persistent kernel launched cooperatively (all
+ * CTAs resident), whose down-projection phase streams Wd while the gate/up
+ * phase finishes and reads each k-block of A as soon as the CTA that wrote
+ * it sets that block's bit in a ready mask; on = 0 (the default) as two
+ * kernels (gate/up, then the down projection as a programmatic dependent
+ * launch).  The fused form is used only when its grid fits the device at
+ * once.  Both forms split the work alike and give the same bits; a
+ * workspace sized by swiglu_mlp_workspace_bytes() fits both.  Returns the
+ * previous setting. */
+int swiglu_mlp_set_nograd_fused(int on);
 
 /* Number of kernels the last fwd / fwd_nograd / bwd call launched on the
  * device (for launch accounting in benchmarks). */

@@ -92,3 +92,17 @@ def test_empty_batch_is_ok_without_launch(L):
 def test_wait_limit_setter(L):
     old = api.swiglu_mlp_set_wait_limit_ns(5)
     assert api.swiglu_mlp_set_wait_limit_ns(old) == 1000  # clamped to 1 us
+
+
+def test_graph_entry_points_check_arguments_first(L):
+    h = ctypes.c_void_p(0)
+    cg = L.swiglu_mlp_graph_create_fwd_nograd
+    assert cg(P, P, P, P, P, 4, 64, 128, 0, P, BIG, None) == INVALID
+    assert cg(N, P, P, P, P, 4, 64, 128, 0, P, BIG, ctypes.byref(h)) == INVALID
+    assert cg(P, P, P, P, P, 4, 60, 128, 0, P, BIG, ctypes.byref(h)) == ALIGN
+    assert cg(P, P, P, P, P_MIS, 4, 64, 128, 0, P, BIG, ctypes.byref(h)) == ALIGN
+    assert cg(P, P, P, P, P, 4, 64, 128, 0, P, 8, ctypes.byref(h)) == WSERR
+    assert cg(P, P, P, P, P, 4, 64, 128, 7, P, BIG, ctypes.byref(h)) == INVALID
+    assert h.value is None  # nothing was created
+    assert L.swiglu_mlp_graph_launch(N, N) == INVALID
+    assert L.swiglu_mlp_graph_destroy(N) == INVALID

@@ -287,9 +287,18 @@ def test_nograd_sweep_parity(S):
     assert within_ulp_frac(f64(A[rt]), r["A"], "bf16") >= 0.99
 
 
+@pytest.fixture(params=[1, 0], ids=["fused", "two_kernels"])
+def ng_mode(request):
+    """Runs a test with the few-token no-grad forward as one fused kernel,
+    then as two kernels."""
+    old = api.swiglu_mlp_set_nograd_fused(bool(request.param))
+    yield request.param
+    api.swiglu_mlp_set_nograd_fused(bool(old))
+
+
 @pytest.mark.parametrize("dtn", ["bf16", "f16"])
 @pytest.mark.parametrize("M", [1, 5, 16, 17, 33, 64])
-def test_nograd_small_m_parity(M, dtn):
+def test_nograd_small_m_parity(M, dtn, ng_mode):
     """Few-token no-grad path (split contraction, per-tile reduction): ragged
     hidden and feature tiles, several splits per tile, against the oracle and
     against the training forward; two calls give the same bits."""
@@ -306,6 +315,78 @@ def test_nograd_small_m_parity(M, dtn):
     assert oracle.rel_frob(f64(A), r["A"]) <= TOL[dtn]
     assert within_ulp_frac(f64(A), r["A"], dtn) >= 0.99
     assert oracle.rel_frob(f64(Y), f64(Yt)) <= TOL[dtn]
+
+
+@pytest.mark.parametrize("M,D,H", [(1, 4096, 11008), (16, 4096, 11008), (33, 4096, 11008),
+                                   (7, 1024, 2816), (64, 2048, 5632), (3, 64, 176),
+                                   (16, 8, 8)])
+def test_nograd_fused_equals_two_kernels_bitwise(M, D, H):
+    """The fused kernel splits both GEMMs exactly as the two kernels do and
+    sums partials in the same order, so the two forms agree bit for bit; the
+    fused one is a single launch."""
+    t = synthetic.make_inputs(M, D, H, "bf16", seed=40 + M, device="cuda", kind="device")
+    old = api.swiglu_mlp_set_nograd_fused(True)
+    try:
+        Yf, Af = api.swiglu_mlp_fwd_nograd(t["X"], t["Wgu"], t["Wd"])
+        n_fused = api.swiglu_mlp_last_launch_count()
+        api.swiglu_mlp_set_nograd_fused(False)
+        Y2, A2 = api.swiglu_mlp_fwd_nograd(t["X"], t["Wgu"], t["Wd"])
+        n_two = api.swiglu_mlp_last_launch_count()
+    finally:
+        api.swiglu_mlp_set_nograd_fused(bool(old))
+    torch.cuda.synchronize()
+    assert (n_fused, n_two) == (1, 2)
+    assert torch.equal(Af, A2)
+    assert torch.equal(Yf, Y2)
+
+
+def test_nograd_fused_reused_workspace_and_mixed_calls():
+    """One workspace serves fused calls, two-kernel calls and training calls
+    in any order: the ready mask and counters are left clear after each."""
+    M, D, H = 16, 1024, 2816
+    t = synthetic.make_inputs(M, D, H, "bf16", seed=50, device="cuda", kind="device")
+    need = max(api.lib().swiglu_mlp_workspace_bytes(M, D, H, 0, op) for op in (0, 1))
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    old = api.swiglu_mlp_set_nograd_fused(True)
+    try:
+        for step in range(6):
+            api.swiglu_mlp_set_nograd_fused(step % 3 != 1)
+            if step == 3:
+                api.swiglu_mlp_fwd(t["X"], t["Wgu"], t["Wd"], ws=ws)
+            x = t["X"] if step % 2 == 0 else torch.randn(M, D, device="cuda").bfloat16()
+            Y, _ = api.swiglu_mlp_fwd_nograd(x, t["Wgu"], t["Wd"], ws=ws)
+            Yr, _ = api.swiglu_mlp_fwd_nograd(x, t["Wgu"], t["Wd"])
+            torch.cuda.synchronize()
+            assert torch.equal(Y, Yr), step
+            assert api.swiglu_mlp_query_error(ws) == 0
+    finally:
+        api.swiglu_mlp_set_nograd_fused(bool(old))
+
+
+def test_nograd_fused_unraised_flag_times_out_cleanly():
+    """Failure detection of the fused kernel's cross-CTA wait without a fault:
+    the first gate/up tile's ready bit is never set, the bounded waits on
+    it run out, the kernel records a timeout and returns; the next call on a
+    fresh workspace is correct."""
+    M, D, H = 16, 320, 392
+    t = synthetic.make_inputs(M, D, H, "bf16", seed=51, device="cuda")
+    ws = api.workspace(M, D, H, torch.bfloat16, api.SWIGLU_OP_FWD_NOGRAD, "cuda")
+    old_mode = api.swiglu_mlp_set_nograd_fused(True)
+    old = api.swiglu_mlp_set_wait_limit_ns(20_000_000)  # 20 ms
+    try:
+        api.swiglu_mlp_inject_stall_once(True)
+        api.swiglu_mlp_fwd_nograd(t["X"], t["Wgu"], t["Wd"], ws=ws)
+        assert api.swiglu_mlp_query_error(ws) == 6
+        Y, A = api.swiglu_mlp_fwd_nograd(t["X"], t["Wgu"], t["Wd"])
+        torch.cuda.synchronize()
+    finally:
+        api.swiglu_mlp_inject_stall_once(False)
+        api.swiglu_mlp_set_wait_limit_ns(old)
+        api.swiglu_mlp_set_nograd_fused(bool(old_mode))
+    c = {k: v.cpu() for k, v in t.items()}
+    r = oracle.forward(c["X"], c["Wg"], c["Wu"], c["Wd"], dt=ODT["bf16"])
+    assert oracle.rel_frob(f64(Y), r["Y"]) <= TOL["bf16"]
+    assert oracle.rel_frob(f64(A), r["A"]) <= TOL["bf16"]
 
 
 def test_stream_k_shared_tiles_parity_and_determinism(cta_pairs):
