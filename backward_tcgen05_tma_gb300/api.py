@@ -294,10 +294,10 @@ def swiglu_mlp_set_cta_pairs(mode: int = 1) -> int:
     return int(lib().swiglu_mlp_set_cta_pairs(int(mode)))
 
 
-def swiglu_mlp_set_nograd_fused(on: bool = True) -> int:
-    """Few-token no-grad calls as one fused kernel (True) or two kernels;
-    returns the previous setting."""
-    return int(lib().swiglu_mlp_set_nograd_fused(1 if on else 0))
+def swiglu_mlp_set_nograd_fused(mode: int = 1) -> int:
+    """Few-token no-grad calls: 0 two kernels, 1 the fused kernel for 33..64
+    tokens (the default), 2 always the fused kernel; returns the previous mode."""
+    return int(lib().swiglu_mlp_set_nograd_fused(int(mode)))
 
 
 def swiglu_mlp_profile_enable(on: bool = True) -> None:

@@ -192,8 +192,8 @@ __device__ __forceinline__ void ng_store_whole(const NgArgs& a, int tile, uint32
   }
 }
 
-// The accumulator as an fp32 partial tile [128][NT] at ``dst`` (then made
-// visible GPU-wide).
+// The accumulator as an fp32 partial tile [128][NT] at ``dst``.  Callers
+// publish it with one release after a barrier over the 128 threads.
 template <int NT>
 __device__ __forceinline__ void ng_store_partial(float* dst, uint32_t tacc, uint32_t acce) {
   const int row = (threadIdx.x & 96) + (threadIdx.x & 31);
@@ -212,8 +212,7 @@ __device__ __forceinline__ void ng_store_partial(float* dst, uint32_t tacc, uint
                       __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
   }
   tc_fence_before();
-  mbar_arrive(acce);  // accumulator free for the unit after next
-  __threadfence();
+  mbar_arrive(acce);  // accumulator free for a later unit
 }
 
 // Sums the n partial tiles part_of(0), ..., part_of(n-1) in that order and
@@ -333,6 +332,7 @@ __device__ __forceinline__ bool ng_epilogue_segment(const NgArgs& a, int tile, b
   epi_bar_sync();
   if (e == 0) {
     int last = 0;
+    __threadfence();  // the 128 threads' partial stores before the count
     if (!*abort_flag) last = atomicAdd(a.counters + tile, 1) == nparts - 1;
     *last_flag = last;
   }

@@ -40,7 +40,7 @@ swiglu_status cuda_status(cudaError_t e);
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_last_launches{0};
 std::atomic<int> g_cta_pairs{1};  // SM pairs (cta_group::2): 0 never, 1 by size, 2 always
-std::atomic<int> g_ng_fused{0};   // few-token no-grad: 1 one fused kernel, 0 two kernels
+std::atomic<int> g_ng_fused{1};   // few-token no-grad: fused kernel 0 never, 1 by size, 2 always
 constexpr int TC2_STAGES = 6;
 
 // ---------------------------------------------------------------------------
@@ -432,30 +432,59 @@ void ng_grid(int tiles, int kb, int& ctas, int& sk_tiles, int& seg_max) {
   ng_split(tiles, kb, ng_max_grid(), ctas, sk_tiles, seg_max);
 }
 
-// The fused kernel's one grid and each phase's split of it.
-struct NgFusedPlan {
-  int grid;
-  int c0, sk0, seg0;  // gate/up
-  int c1, sk1, seg1;  // down
+// The fused kernel's work units.  gate/up: runs of 64 k-blocks (the
+// gate/up units all precede the down units, so their end overlaps the down
+// units' start); down: runs of 32 k-blocks, then 16 and 8 over the last
+// 2 x 32 k-blocks, so the last units handed out are short.  Per unit the
+// epilogue writes a partial tile of 128 x NT fp32 (at most an eighth of the
+// unit's weight bytes).  A GEMM whose k-blocks fit one run has whole tiles
+// (no partials).  Measured on D = 4096, H = 11008: this pair beat 16 / 32-
+// and 8 / 16-k-block units, with and without the taper, at 1 and 64 tokens.
+struct NgDynPlan {
+  int chunks0, chunks1, units0, units1, grid;
+  int kb_at[2][NG_MAX_CHUNKS + 1];
   size_t part0_bytes, part1_bytes;
 };
 
-NgFusedPlan ng_fused_plan(const NgPlan& p) {
-  NgFusedPlan f;
-  const int g = ng_max_grid();
-  ng_split(p.t1, p.kb1, g, f.c0, f.sk0, f.seg0);
-  ng_split(p.t2, p.kb2, g, f.c1, f.sk1, f.seg1);
-  f.grid = f.c0 > f.c1 ? f.c0 : f.c1;
-  f.part0_bytes = (size_t)f.c0 * f.seg0 * 128 * p.NT * 4;
-  f.part1_bytes = (size_t)f.c1 * f.seg1 * 128 * p.NT * 4;
-  return f;
+int ng_chunks(int kb, int q, bool taper, int* at) {
+  int n = 0, k = 0;
+  at[0] = 0;
+  while (k < kb) {
+    const int rem = kb - k;
+    int len = q;
+    if (taper && rem <= 2 * q) len = rem > q ? q / 2 : q / 4;
+    if (len < 1) len = 1;
+    if (len > rem) len = rem;
+    // the table has NG_MAX_CHUNKS entries: the last one takes the rest
+    if (n == NG_MAX_CHUNKS - 1) len = rem;
+    k += len;
+    at[++n] = k;
+  }
+  return n;
 }
 
-// Workspace bytes of the fused kernel on the current device: both phases'
-// partial tiles are live at once.
+NgDynPlan ng_dyn_plan(const NgPlan& p) {
+  NgDynPlan d;
+  int q0 = 64, q1 = 32;
+  // keep at most NG_MAX_CHUNKS runs per tile on very long contractions
+  while ((p.kb1 + q0 - 1) / q0 > NG_MAX_CHUNKS / 2) q0 *= 2;
+  while ((p.kb2 + q1 - 1) / q1 > NG_MAX_CHUNKS / 2) q1 *= 2;
+  d.chunks0 = ng_chunks(p.kb1, q0, false, d.kb_at[0]);
+  d.chunks1 = ng_chunks(p.kb2, q1, true, d.kb_at[1]);
+  d.units0 = p.t1 * d.chunks0;
+  d.units1 = p.t2 * d.chunks1;
+  const int g = ng_max_grid();
+  const int units = d.units0 + d.units1;
+  d.grid = units < g ? units : g;
+  d.part0_bytes = d.chunks0 > 1 ? (size_t)d.units0 * 128 * p.NT * 4 : 0;
+  d.part1_bytes = d.chunks1 > 1 ? (size_t)d.units1 * 128 * p.NT * 4 : 0;
+  return d;
+}
+
+// Workspace bytes of the fused kernel: one partial slot per unit.
 size_t ng_fused_bytes(const NgPlan& p) {
-  const NgFusedPlan f = ng_fused_plan(p);
-  return WS_HEADER + p.counter_bytes + f.part0_bytes + f.part1_bytes;
+  const NgDynPlan d = ng_dyn_plan(p);
+  return WS_HEADER + p.counter_bytes + d.part0_bytes + d.part1_bytes;
 }
 
 // Workspace bytes of the two-kernel form with the current device's grids
@@ -527,83 +556,76 @@ swiglu_status ng_forward_nt(const void* X, const void* Wgu, const void* Wd, void
 }
 
 constexpr size_t NG_DONE_OFFSET = 128;  // the fused kernel's finished-CTA count (header)
+constexpr size_t NG_NEXT_OFFSET = 192;  // the fused kernel's work-queue counter (header)
 
-// Whether the fused kernel's grid can be resident all at once on the current
-// device (queried once per device).
-template <int NT, bool BF16>
-bool ng_fused_fits(int grid) {
-  static std::mutex mu;
-  static int cached[64];  // 0 unknown, else 1 + blocks per SM
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  std::lock_guard<std::mutex> g(mu);
-  if (cached[dev] == 0) {
-    auto kern = ng_fused_kernel<NT, BF16>;
-    constexpr int smem = NgSmem<NT>::DYN_BYTES;
-    int nb = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, NG_THREADS, smem) !=
-            cudaSuccess) {
-      cudaGetLastError();
-      nb = 0;
-    }
-    cached[dev] = 1 + nb;
-  }
-  return (int64_t)(cached[dev] - 1) * sm_count() >= grid;
-}
-
-// The fused form: one cooperative launch for both GEMMs.  ws layout as for
-// the two kernels, plus the ready mask after the counters, the finished-CTA
-// count in the header, and the two phases' partial tiles side by side.
+// The fused form: one launch for both GEMMs with a dynamic work queue.  ws
+// layout as for the two kernels (header, per-tile counters of both GEMMs),
+// plus the ready mask after the counters, the queue counter and the
+// finished-CTA count in the header, and one partial slot per unit.
 template <int NT, bool BF16>
 swiglu_status ng_forward_fused(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
                                int64_t M, int64_t D, int64_t H, const NgPlan& p, char* ws,
                                cudaStream_t st) {
-  const NgFusedPlan fp = ng_fused_plan(p);
+  auto kern = ng_fused_kernel<NT, BF16>;
+  constexpr int smem = NgDynSmem<NT>::DYN_BYTES;
+  {
+    static std::mutex mu;
+    static bool set[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SWIGLU_ERR_CUDA;
+    std::lock_guard<std::mutex> g(mu);
+    if (!set[dev]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess)
+        return SWIGLU_ERR_CUDA;
+      set[dev] = true;
+    }
+  }
+  const NgDynPlan d = ng_dyn_plan(p);
   int* err = reinterpret_cast<int*>(ws);
   int* counters = reinterpret_cast<int*>(ws + WS_HEADER);
-  NgFusedArgs f;
+  NgDynArgs f;
+  f.chunks[0] = d.chunks0;
+  f.chunks[1] = d.chunks1;
+  std::memcpy(f.kb_at, d.kb_at, sizeof(f.kb_at));
+  f.units0 = d.units0;
+  f.units = d.units0 + d.units1;
   f.ready = reinterpret_cast<uint32_t*>(counters + p.t1 + p.t2);
+  f.next_unit = reinterpret_cast<uint32_t*>(ws + NG_NEXT_OFFSET);
   f.done = reinterpret_cast<uint32_t*>(ws + NG_DONE_OFFSET);
   f.inject_unready = g_inject_stall.exchange(0);
   float* part0 = reinterpret_cast<float*>(ws + WS_HEADER + p.counter_bytes);
-  float* part1 = reinterpret_cast<float*>(ws + WS_HEADER + p.counter_bytes + fp.part0_bytes);
+  float* part1 = reinterpret_cast<float*>(ws + WS_HEADER + p.counter_bytes + d.part0_bytes);
   const uint64_t wl = g_wait_limit_ns.load();
   CUtensorMap twgu, tx, twd, ta;
   if (!encode_gateup(&twgu, BF16, Wgu, D, H, 64) || !map_kmajor(&tx, BF16, X, D, M, D, NT) ||
       !map_kmajor(&twd, BF16, Wd, H, D, H, 128) || !map_kmajor(&ta, BF16, A, H, M, H, NT))
     return SWIGLU_ERR_CUDA;
-  f.ph[0] = NgArgs{(int)M, (int)H, p.kb1, p.t1, fp.sk0, fp.seg0, part0, counters, nullptr, 0, 1,
-                   0, fp.c0, A, H, wl, err};
-  f.ph[1] = NgArgs{(int)M, (int)D, p.kb2, p.t2, fp.sk1, fp.seg1, part1, counters + p.t1, nullptr,
-                   0, 0, 0, fp.c1, Y, D, wl, err};
-  auto kern = ng_fused_kernel<NT, BF16>;
+  f.ph[0] = NgArgs{(int)M, (int)H, p.kb1, p.t1, 0, 0, part0, counters, nullptr, 0, 1, 0, 0,
+                   A, H, wl, err};
+  f.ph[1] = NgArgs{(int)M, (int)D, p.kb2, p.t2, 0, 0, part1, counters + p.t1, nullptr, 0, 0, 0,
+                   0, Y, D, wl, err};
   ProfScope prof(K_NG_FUSED, st);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)fp.grid);
+  cfg.gridDim = dim3((unsigned)d.grid);
   cfg.blockDim = dim3(NG_THREADS);
-  cfg.dynamicSmemBytes = NgSmem<NT>::DYN_BYTES;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // phase 1 waits on flags other CTAs raise
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, twgu, tx, twd, ta, f);
   g_last_launches.fetch_add(1);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   return cuda_status(cudaGetLastError());
 }
 
-// The fused form when it is enabled and its grid fits the device (and,
-// for a fixed scratch array, its workspace fits `ws_cap`), else two kernels.
+// The fused form when it is selected (by default for 33..64 tokens, where
+// it measured faster; for fewer tokens both forms take the same time) and,
+// for a fixed scratch array, its workspace fits `ws_cap`; else two kernels.
 template <int NT, bool BF16>
 swiglu_status ng_forward_t(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
                            int64_t M, int64_t D, int64_t H, const NgPlan& p, char* ws,
                            size_t ws_cap, cudaStream_t st) {
-  if (g_ng_fused.load() != 0 && ng_fused_bytes(p) <= ws_cap &&
-      ng_fused_fits<NT, BF16>(ng_fused_plan(p).grid))
+  const int mode = g_ng_fused.load();
+  if ((mode == 2 || (mode == 1 && NT == 64)) && ng_fused_bytes(p) <= ws_cap)
     return ng_forward_fused<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, st);
   if (ng_two_bytes(p) > ws_cap) return SWIGLU_ERR_UNSUPPORTED;
   return ng_forward_nt<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, st);
@@ -909,8 +931,7 @@ swiglu_status swiglu_mlp_fwd_nograd_noalloc(const void* X, const void* Wgu, cons
   void* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != SWIGLU_OK) return st;
   const NgPlan p = ng_plan(M, D, H);
-  if (ng_two_bytes(p) > NOALLOC_SCRATCH_BYTES &&
-      (g_ng_fused.load() == 0 || ng_fused_bytes(p) > NOALLOC_SCRATCH_BYTES))
+  if (ng_two_bytes(p) > NOALLOC_SCRATCH_BYTES && ng_fused_bytes(p) > NOALLOC_SCRATCH_BYTES)
     return SWIGLU_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: clear the error word, the
@@ -1057,7 +1078,9 @@ void swiglu_mlp_inject_stall_once(int on) { g_inject_stall.store(on ? 1 : 0); }
 
 int swiglu_mlp_last_launch_count(void) { return g_last_launches.load(); }
 
-int swiglu_mlp_set_nograd_fused(int on) { return g_ng_fused.exchange(on ? 1 : 0); }
+int swiglu_mlp_set_nograd_fused(int mode) {
+  return g_ng_fused.exchange(mode <= 0 ? 0 : (mode >= 2 ? 2 : 1));
+}
 
 int swiglu_mlp_set_cta_pairs(int mode) {
   return g_cta_pairs.exchange(mode <= 0 ? 0 : (mode >= 2 ? 2 : 1));

@@ -231,16 +231,19 @@ void swiglu_mlp_inject_stall_once(int on);
 int swiglu_mlp_set_cta_pairs(int mode);
 
 /* Selects how later few-token no-grad calls (M <= 64, bf16/fp16) of this
- * process run: on = 1 as ONE persistent kernel launched cooperatively (all
- * CTAs resident), whose down-projection phase streams Wd while the gate/up
- * phase finishes and reads each k-block of A as soon as the CTA that wrote
- * it sets that block's bit in a ready mask; on = 0 (the default) as two
- * kernels (gate/up, then the down projection as a programmatic dependent
- * launch).  The fused form is used only when its grid fits the device at
- * once.  Both forms split the work alike and give the same bits; a
- * workspace sized by swiglu_mlp_workspace_bytes() fits both.  Returns the
- * previous setting. */
-int swiglu_mlp_set_nograd_fused(int on);
+ * process run: as ONE persistent kernel that hands out fixed work units (a
+ * gate/up or down tile x a run of k-blocks) from a queue in the workspace,
+ * so faster SMs take more of the weight stream, and that starts each
+ * down-projection k-block as soon as the A columns it reads are written (a
+ * ready mask in the workspace); or as two kernels (gate/up, then the down
+ * projection as a programmatic dependent launch).  mode 0: always two
+ * kernels; 1 (the default): the fused kernel for 33..64 tokens, where it is
+ * faster, two kernels below; 2: always the fused kernel.  Both forms are
+ * deterministic (partial sums are added in a fixed order); they split the
+ * contractions at different points, so their results differ in rounding
+ * only.  A workspace sized by swiglu_mlp_workspace_bytes() fits both.
+ * Returns the previous mode. */
+int swiglu_mlp_set_nograd_fused(int mode);
 
 /* Number of kernels the last fwd / fwd_nograd / bwd call launched on the
  * device (for launch accounting in benchmarks). */

@@ -48,8 +48,7 @@ def _noalloc(L, t, M, D, H, dt):
                                        ("bf16", 32, 4096, 11008), ("f16", 5, 320, 392),
                                        ("bf16", 32, 512, 1024), ("bf16", 64, 4096, 11008)])
 def test_noalloc_matches_workspace_entry_point(L, dtn, M, D, H):
-    # M = 64 at D = 4096, H = 11008: the fused kernel's partial tiles exceed
-    # the array, so the call runs as two kernels
+    # M = 33..64 runs the fused kernel by default, fewer tokens two kernels
     dt = {"bf16": 0, "f16": 1}[dtn]
     t = synthetic.make_inputs(M, D, H, dtn, seed=M, device="cuda", kind="device")
     Y_ref, A_ref = api.swiglu_mlp_fwd_nograd(t["X"], t["Wgu"], t["Wd"])
