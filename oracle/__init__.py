@@ -10,7 +10,9 @@ so that the same source gives the same fp64 results on x86 and on Arm.
 This module is argument marshalling around it, plus ``rel_frob``.
 
 Sources: "[RFC] Full-pipeline SwiGLU MLP with forward/backward
-co-optimization" (Liger-Kernel #1347), sections "Summary" and "Correctness";
+co-optimization" (Liger-Kernel #1347), sections "Summary" and "Correctness",
+and its maintainer thread (the gate/down multiplier variant deferred to a
+follow-up; the reading taken is stated in swiglu_oracle.c);
 "Scope one-round FP32 SwiGLU to the exact Qwen3.5 contract" (xorl #51),
 review section (one-round vs two-round programs).
 """
@@ -63,9 +65,14 @@ def _load():
             getattr(lib, name).argtypes = [ctypes.c_double]
         lib.oracle_decode.argtypes = [vp, ci, i64, dp]
         lib.oracle_round_array.argtypes = [dp, ci, i64, dp]
+        cd = ctypes.c_double
         lib.oracle_fwd.argtypes = [vp, vp, vp, vp, ci, i64, i64, i64, ci, ci, dp, dp, dp, dp]
+        lib.oracle_fwd_ex.argtypes = [vp, vp, vp, vp, ci, i64, i64, i64, ci, ci, cd, cd,
+                                      dp, dp, dp, dp]
         lib.oracle_bwd.argtypes = [vp, vp, vp, vp, vp, ci, dp, dp, dp, i64, i64, i64, ci, ci,
                                    dp, dp, dp, dp, dp, dp]
+        lib.oracle_bwd_ex.argtypes = [vp, vp, vp, vp, vp, ci, dp, dp, dp, i64, i64, i64, ci, ci,
+                                      cd, cd, dp, dp, dp, dp, dp, dp, dp, dp, dp]
         lib.oracle_rows.argtypes = [vp, vp, vp, vp, vp, ci, i64, i64, i64, vp, i64, ci, ci,
                                     dp, dp, dp, dp, dp, dp, dp]
         lib.oracle_cols.argtypes = [vp, vp, vp, vp, vp, ci, i64, i64, i64, vp, i64, ci, ci,
@@ -146,8 +153,11 @@ def sigmoid(g: float) -> float:
     return _load().oracle_sigmoid(float(g))
 
 
-def forward(X, Wg, Wu, Wd, mode: int = ONE_ROUND, dt: int | None = None):
-    """Full forward.  Returns dict of fp64 arrays G, U, A [M,H] and Y [M,D]."""
+def forward(X, Wg, Wu, Wd, mode: int = ONE_ROUND, dt: int | None = None,
+            gate_mul: float = 1.0, down_mul: float = 1.0):
+    """Full forward.  Returns dict of fp64 arrays G, U, A [M,H] and Y [M,D].
+    ``gate_mul`` / ``down_mul``: A = SiLU(gate_mul X Wg^T) U, Y = down_mul A Wd^T
+    (G is then the stored pre-activation gate_mul X Wg^T)."""
     lib = _load()
     (X, Wg, Wu, Wd), in_dt = _inputs(X, Wg, Wu, Wd)
     dt = in_dt if dt is None else dt
@@ -155,14 +165,17 @@ def forward(X, Wg, Wu, Wd, mode: int = ONE_ROUND, dt: int | None = None):
     H = Wg.shape[0]
     assert Wg.shape == (H, D) and Wu.shape == (H, D) and Wd.shape == (D, H)
     G = np.empty((M, H)); U = np.empty((M, H)); A = np.empty((M, H)); Y = np.empty((M, D))
-    lib.oracle_fwd(_ptr(X), _ptr(Wg), _ptr(Wu), _ptr(Wd), in_dt, M, D, H, mode, dt,
-                   _ptr(G), _ptr(U), _ptr(A), _ptr(Y))
+    lib.oracle_fwd_ex(_ptr(X), _ptr(Wg), _ptr(Wu), _ptr(Wd), in_dt, M, D, H, mode, dt,
+                      float(gate_mul), float(down_mul), _ptr(G), _ptr(U), _ptr(A), _ptr(Y))
     return {"G": G, "U": U, "A": A, "Y": Y}
 
 
-def backward(dY, X, Wg, Wu, Wd, fwd: dict, mode: int = ONE_ROUND, dt: int | None = None):
+def backward(dY, X, Wg, Wu, Wd, fwd: dict, mode: int = ONE_ROUND, dt: int | None = None,
+             gate_mul: float = 1.0, down_mul: float = 1.0, accumulate: dict | None = None):
     """Full backward from the oracle's own stored forward values ``fwd``.
-    Returns dict of fp64 arrays dG, dU, dX, dWg, dWu, dWd."""
+    Returns dict of fp64 arrays dG, dU, dX, dWg, dWu, dWd.  ``accumulate``:
+    the weight gradients already held ({"dWg", "dWu", "dWd"}, fp64 values),
+    to which the new ones are added with one rounding; None overwrites."""
     lib = _load()
     (dY, X, Wg, Wu, Wd), in_dt = _inputs(dY, X, Wg, Wu, Wd)
     dt = in_dt if dt is None else dt
@@ -173,10 +186,18 @@ def backward(dY, X, Wg, Wu, Wd, fwd: dict, mode: int = ONE_ROUND, dt: int | None
     A = np.ascontiguousarray(fwd["A"], dtype=np.float64)
     out = {k: np.empty(s) for k, s in (("dG", (M, H)), ("dU", (M, H)), ("dX", (M, D)),
                                          ("dWg", (H, D)), ("dWu", (H, D)), ("dWd", (D, H)))}
-    lib.oracle_bwd(_ptr(dY), _ptr(X), _ptr(Wg), _ptr(Wu), _ptr(Wd), in_dt,
-                   _ptr(G), _ptr(U), _ptr(A), M, D, H, mode, dt,
-                   _ptr(out["dG"]), _ptr(out["dU"]), _ptr(out["dX"]),
-                   _ptr(out["dWg"]), _ptr(out["dWu"]), _ptr(out["dWd"]))
+    acc = {}
+    null = ctypes.c_void_p(0)
+    for k, shape in (("dWg", (H, D)), ("dWu", (H, D)), ("dWd", (D, H))):
+        if accumulate is not None:
+            acc[k] = np.ascontiguousarray(accumulate[k], dtype=np.float64)
+            assert acc[k].shape == shape
+    ap = {k: (_ptr(acc[k]) if k in acc else null) for k in ("dWg", "dWu", "dWd")}
+    lib.oracle_bwd_ex(_ptr(dY), _ptr(X), _ptr(Wg), _ptr(Wu), _ptr(Wd), in_dt,
+                      _ptr(G), _ptr(U), _ptr(A), M, D, H, mode, dt, float(gate_mul),
+                      float(down_mul), ap["dWg"], ap["dWu"], ap["dWd"],
+                      _ptr(out["dG"]), _ptr(out["dU"]), _ptr(out["dX"]),
+                      _ptr(out["dWg"]), _ptr(out["dWu"]), _ptr(out["dWd"]))
     return out
 
 

@@ -26,6 +26,16 @@
  *   - backward uses the stored (rounded) G, U, A; dA is never rounded;
  *   - gradients are rounded once to the storage type.
  *
+ *   Gate/down multipliers (the Falcon-H1 variant the maintainer thread of
+ *   the RFC defers to a follow-up, "[RFC] Full-pipeline SwiGLU MLP ...",
+ *   maintainer thread; the pages do not define it, the plain reading is
+ *   taken):  A = SiLU(mg G) * U,  Y = md (A Wd^T), G = X Wg^T, U = X Wu^T;
+ *   the stored gate pre-activation is mg G.  By the chain rule
+ *       dA = md (dY Wd),  dU = dA SiLU(mg G),  dG = dA U SiLU'(mg G) mg,
+ *       dWd = md (dY^T A),  dWg = dG^T X,  dWu = dU^T X,  dX = dG Wg + dU Wu.
+ *   mg = md = 1 is the standard MLP.  Gradient accumulation (beta = 1):
+ *   dW = rnd(dW_before + the new sum), one rounding.
+ *
  * Modes:
  *   ORACLE_EXACT     fp64 throughout, nothing rounded (finite differences);
  *   ORACLE_ONE_ROUND rounds at the same points as the GPU path (parity);
@@ -132,9 +142,9 @@ double oracle_dsilu(double g) {
 /* ---------------------------------------------------------------------- */
 
 /* One row of the gate/up stage: for hidden unit j,
- *   g = sum_k X[m,k] Wg[j,k],  u = sum_k X[m,k] Wu[j,k]. */
+ *   g = mg * sum_k X[m,k] Wg[j,k],  u = sum_k X[m,k] Wu[j,k]. */
 static void gate_up_row(const void* X, const void* Wg, const void* Wu, int in_dt,
-                        int64_t m, int64_t D, int64_t H, int mode, int dt,
+                        int64_t m, int64_t D, int64_t H, int mode, int dt, double mg,
                         double* Grow, double* Urow, double* Arow) {
   for (int64_t j = 0; j < H; ++j) {
     double g = 0.0, u = 0.0;
@@ -143,6 +153,7 @@ static void gate_up_row(const void* X, const void* Wg, const void* Wu, int in_dt
       g += x * load_elem(Wg, j * D + k, in_dt);
       u += x * load_elem(Wu, j * D + k, in_dt);
     }
+    g = mg * g;
     double gs = rnd(g, mode, dt), us = rnd(u, mode, dt);
     double a;
     if (mode == ORACLE_TWO_ROUND)
@@ -155,67 +166,83 @@ static void gate_up_row(const void* X, const void* Wg, const void* Wu, int in_dt
   }
 }
 
-/* Y[m,d] = sum_j A[m,j] Wd[d,j]. */
+/* Y[m,d] = md * sum_j A[m,j] Wd[d,j]. */
 static void down_row(const double* Arow, const void* Wd, int in_dt, int64_t D, int64_t H,
-                     int mode, int dt, double* Yrow) {
+                     int mode, int dt, double md, double* Yrow) {
   for (int64_t d = 0; d < D; ++d) {
     double y = 0.0;
     for (int64_t j = 0; j < H; ++j) y += Arow[j] * load_elem(Wd, d * H + j, in_dt);
-    Yrow[d] = rnd(y, mode, dt);
+    Yrow[d] = rnd(md * y, mode, dt);
   }
 }
 
-/* X [M,D], Wg/Wu [H,D], Wd [D,H] in storage type in_dt (row-major).
- * Outputs (fp64, row-major): G, U, A [M,H] (G/U may be NULL), Y [M,D]. */
+/* X [M,D], Wg/Wu [H,D], Wd [D,H] in storage type in_dt (row-major); gate and
+ * down multipliers mg, md.  Outputs (fp64, row-major): G (the stored gate
+ * pre-activation mg X Wg^T), U, A [M,H] (G/U may be NULL), Y [M,D]. */
+void oracle_fwd_ex(const void* X, const void* Wg, const void* Wu, const void* Wd, int in_dt,
+                   int64_t M, int64_t D, int64_t H, int mode, int dt, double mg, double md,
+                   double* G, double* U, double* A, double* Y) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t m = 0; m < M; ++m) {
+    gate_up_row(X, Wg, Wu, in_dt, m, D, H, mode, dt, mg,
+                G ? G + m * H : NULL, U ? U + m * H : NULL, A + m * H);
+    down_row(A + m * H, Wd, in_dt, D, H, mode, dt, md, Y + m * D);
+  }
+}
+
+/* The standard MLP: mg = md = 1. */
 void oracle_fwd(const void* X, const void* Wg, const void* Wu, const void* Wd, int in_dt,
                 int64_t M, int64_t D, int64_t H, int mode, int dt,
                 double* G, double* U, double* A, double* Y) {
-#pragma omp parallel for schedule(dynamic, 1)
-  for (int64_t m = 0; m < M; ++m) {
-    gate_up_row(X, Wg, Wu, in_dt, m, D, H, mode, dt,
-                G ? G + m * H : NULL, U ? U + m * H : NULL, A + m * H);
-    down_row(A + m * H, Wd, in_dt, D, H, mode, dt, Y + m * D);
-  }
+  oracle_fwd_ex(X, Wg, Wu, Wd, in_dt, M, D, H, mode, dt, 1.0, 1.0, G, U, A, Y);
 }
 
 /* ---------------------------------------------------------------------- */
 /* Full backward                                                           */
 /* ---------------------------------------------------------------------- */
 
-/* dA[m,j] = sum_d dY[m,d] Wd[d,j] (kept in fp64, never rounded), then
- *   dU = dA * SiLU(G),  dG = dA * U * SiLU'(G)
- * with G, U the stored values. */
+/* dA[m,j] = md * sum_d dY[m,d] Wd[d,j] (kept in fp64, never rounded), then
+ *   dU = dA * SiLU(G),  dG = dA * U * SiLU'(G) * mg
+ * with G (= mg X Wg^T), U the stored values. */
 static void dgu_row(const void* dY, const void* Wd, int in_dt, const double* Grow,
                     const double* Urow, int64_t m, int64_t D, int64_t H, int mode, int dt,
-                    double* dGrow, double* dUrow) {
+                    double mg, double md, double* dGrow, double* dUrow) {
   for (int64_t j = 0; j < H; ++j) {
     double da = 0.0;
     for (int64_t d = 0; d < D; ++d)
       da += load_elem(dY, m * D + d, in_dt) * load_elem(Wd, d * H + j, in_dt);
+    da = md * da;
     double g = Grow[j], u = Urow[j];
     dUrow[j] = rnd(da * oracle_silu(g), mode, dt);
-    dGrow[j] = rnd(da * u * oracle_dsilu(g), mode, dt);
+    dGrow[j] = rnd(da * u * oracle_dsilu(g) * mg, mode, dt);
   }
 }
 
 /* Inputs: dY [M,D]; X, Wg, Wu, Wd as in oracle_fwd; G, U, A [M,H] the stored
- * forward values (fp64 arrays holding storage-type values).
+ * forward values (fp64 arrays holding storage-type values); multipliers mg,
+ * md as in oracle_fwd_ex; dWg0, dWu0, dWd0: the gradients already held, to
+ * which the new ones are added (beta = 1), or NULL (overwrite).
  * Outputs (fp64): dG, dU [M,H]; dX [M,D]; dWg, dWu [H,D]; dWd [D,H].
  * Separate form: dWg = dG^T X, dWu = dU^T X, dX = dG Wg + dU Wu. */
-void oracle_bwd(const void* dY, const void* X, const void* Wg, const void* Wu,
-                const void* Wd, int in_dt, const double* G, const double* U,
-                const double* A, int64_t M, int64_t D, int64_t H, int mode, int dt,
-                double* dG, double* dU, double* dX, double* dWg, double* dWu, double* dWd) {
+void oracle_bwd_ex(const void* dY, const void* X, const void* Wg, const void* Wu,
+                   const void* Wd, int in_dt, const double* G, const double* U,
+                   const double* A, int64_t M, int64_t D, int64_t H, int mode, int dt,
+                   double mg, double md, const double* dWg0, const double* dWu0,
+                   const double* dWd0, double* dG, double* dU, double* dX, double* dWg,
+                   double* dWu, double* dWd) {
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t m = 0; m < M; ++m)
-    dgu_row(dY, Wd, in_dt, G + m * H, U + m * H, m, D, H, mode, dt, dG + m * H, dU + m * H);
+    dgu_row(dY, Wd, in_dt, G + m * H, U + m * H, m, D, H, mode, dt, mg, md, dG + m * H,
+            dU + m * H);
 
-  /* dWd[d,j] = sum_m dY[m,d] A[m,j] */
+  /* dWd[d,j] = md * sum_m dY[m,d] A[m,j] */
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t d = 0; d < D; ++d)
     for (int64_t j = 0; j < H; ++j) {
       double s = 0.0;
       for (int64_t m = 0; m < M; ++m) s += load_elem(dY, m * D + d, in_dt) * A[m * H + j];
+      s = md * s;
+      if (dWd0) s += dWd0[d * H + j];
       dWd[d * H + j] = rnd(s, mode, dt);
     }
 
@@ -229,6 +256,8 @@ void oracle_bwd(const void* dY, const void* X, const void* Wg, const void* Wu,
         sg += dG[m * H + j] * x;
         su += dU[m * H + j] * x;
       }
+      if (dWg0) sg += dWg0[j * D + k];
+      if (dWu0) su += dWu0[j * D + k];
       dWg[j * D + k] = rnd(sg, mode, dt);
       dWu[j * D + k] = rnd(su, mode, dt);
     }
@@ -244,6 +273,15 @@ void oracle_bwd(const void* dY, const void* X, const void* Wg, const void* Wu,
       }
       dX[m * D + k] = rnd(pg + pu, mode, dt);
     }
+}
+
+/* The standard MLP, gradients overwritten. */
+void oracle_bwd(const void* dY, const void* X, const void* Wg, const void* Wu,
+                const void* Wd, int in_dt, const double* G, const double* U,
+                const double* A, int64_t M, int64_t D, int64_t H, int mode, int dt,
+                double* dG, double* dU, double* dX, double* dWg, double* dWu, double* dWd) {
+  oracle_bwd_ex(dY, X, Wg, Wu, Wd, in_dt, G, U, A, M, D, H, mode, dt, 1.0, 1.0, NULL, NULL,
+                NULL, dG, dU, dX, dWg, dWu, dWd);
 }
 
 /* ---------------------------------------------------------------------- */
@@ -262,9 +300,10 @@ void oracle_rows(const void* X, const void* Wg, const void* Wu, const void* Wd,
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < R; ++r) {
     int64_t m = rows[r];
-    gate_up_row(X, Wg, Wu, in_dt, m, D, H, mode, dt, G_s + r * H, U_s + r * H, A_s + r * H);
-    down_row(A_s + r * H, Wd, in_dt, D, H, mode, dt, Y_s + r * D);
-    dgu_row(dY, Wd, in_dt, G_s + r * H, U_s + r * H, m, D, H, mode, dt,
+    gate_up_row(X, Wg, Wu, in_dt, m, D, H, mode, dt, 1.0, G_s + r * H, U_s + r * H,
+                A_s + r * H);
+    down_row(A_s + r * H, Wd, in_dt, D, H, mode, dt, 1.0, Y_s + r * D);
+    dgu_row(dY, Wd, in_dt, G_s + r * H, U_s + r * H, m, D, H, mode, dt, 1.0, 1.0,
             dG_s + r * H, dU_s + r * H);
     for (int64_t k = 0; k < D; ++k) {
       double pg = 0.0, pu = 0.0;

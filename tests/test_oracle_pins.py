@@ -154,12 +154,13 @@ def test_exact_backward_aggregated_equals_separate(oracle_lib):
     assert oracle.rel_frob(b["dU"], dA * _silu_np(f["G"])) < 1e-12
 
 
-def _loss(x):
-    f = oracle.forward(x["X"], x["Wg"], x["Wu"], x["Wd"], mode=oracle.EXACT)
+def _loss(x, gm=1.0, dm=1.0):
+    f = oracle.forward(x["X"], x["Wg"], x["Wu"], x["Wd"], mode=oracle.EXACT, gate_mul=gm,
+                       down_mul=dm)
     return float(np.sum(x["dY"] * f["Y"]))
 
 
-def _fd_check(x, b, coords_per_tensor=None, seed=0):
+def _fd_check(x, b, coords_per_tensor=None, seed=0, gm=1.0, dm=1.0):
     eps = 1e-6
     grads = {"X": b["dX"], "Wg": b["dWg"], "Wu": b["dWu"], "Wd": b["dWd"]}
     rng = np.random.default_rng(seed)
@@ -172,7 +173,7 @@ def _fd_check(x, b, coords_per_tensor=None, seed=0):
             xp = dict(x); xm = dict(x)
             p = base.copy().ravel(); p[i] += eps; xp[name] = p.reshape(base.shape)
             q = base.copy().ravel(); q[i] -= eps; xm[name] = q.reshape(base.shape)
-            fd = (_loss(xp) - _loss(xm)) / (2 * eps)
+            fd = (_loss(xp, gm, dm) - _loss(xm, gm, dm)) / (2 * eps)
             an = g.ravel()[i]
             assert abs(fd - an) <= 1e-6 * max(abs(an), 1e-3 * scale), (name, i, fd, an)
 
@@ -190,6 +191,91 @@ def test_gradients_match_finite_differences_tiny_config(oracle_lib):
     f = oracle.forward(x["X"], x["Wg"], x["Wu"], x["Wd"], mode=oracle.EXACT)
     b = oracle.backward(x["dY"], x["X"], x["Wg"], x["Wu"], x["Wd"], f, mode=oracle.EXACT)
     _fd_check(x, b, coords_per_tensor=48, seed=1)
+
+
+# --------------------------------------------------------------------------
+# gate/down multipliers and gradient accumulation
+# --------------------------------------------------------------------------
+
+def test_multiplier_forward_matches_numpy_matmul(oracle_lib):
+    # A = SiLU(gm X Wg^T) (X Wu^T), Y = dm A Wd^T, G stored as gm X Wg^T
+    gm, dm = 1.7, 0.6
+    x = _f64_inputs(7, 24, 40, 13)
+    f = oracle.forward(x["X"], x["Wg"], x["Wu"], x["Wd"], mode=oracle.EXACT, gate_mul=gm,
+                       down_mul=dm)
+    G = gm * (x["X"] @ x["Wg"].T)
+    U = x["X"] @ x["Wu"].T
+    A = _silu_np(G) * U
+    for name, ref in (("G", G), ("U", U), ("A", A), ("Y", dm * (A @ x["Wd"].T))):
+        assert oracle.rel_frob(f[name], ref) < 1e-13, name
+
+
+def test_power_of_two_multipliers_equal_scaled_weights(oracle_lib):
+    """mg = 2 is the standard MLP with Wg doubled, md = 1/2 the one with Wd
+    halved: every output agrees bit for bit in exact arithmetic, with
+    dWg = 2 x (gradient w.r.t. the doubled Wg), dWd = 1/2 x (gradient w.r.t.
+    the halved Wd)."""
+    x = _f64_inputs(5, 16, 24, 14)
+    f = oracle.forward(x["X"], x["Wg"], x["Wu"], x["Wd"], mode=oracle.EXACT, gate_mul=2.0,
+                       down_mul=0.5)
+    b = oracle.backward(x["dY"], x["X"], x["Wg"], x["Wu"], x["Wd"], f, mode=oracle.EXACT,
+                        gate_mul=2.0, down_mul=0.5)
+    Wg2, Wd2 = 2.0 * x["Wg"], 0.5 * x["Wd"]
+    fs = oracle.forward(x["X"], Wg2, x["Wu"], Wd2, mode=oracle.EXACT)
+    bs = oracle.backward(x["dY"], x["X"], Wg2, x["Wu"], Wd2, fs, mode=oracle.EXACT)
+    for k in ("G", "U", "A", "Y"):
+        np.testing.assert_array_equal(f[k], fs[k])
+    for k in ("dU", "dX", "dWu"):
+        np.testing.assert_array_equal(b[k], bs[k])
+    np.testing.assert_array_equal(b["dG"], 2.0 * bs["dG"])
+    np.testing.assert_array_equal(b["dWg"], 2.0 * bs["dWg"])
+    np.testing.assert_array_equal(b["dWd"], 0.5 * bs["dWd"])
+
+
+def test_multiplier_gradients_match_finite_differences(oracle_lib):
+    gm, dm = 1.7, 0.6
+    for (M, D, H), coords in (((3, 8, 16), None), ((32, 64, 176), 32)):
+        x = _f64_inputs(M, D, H, 15)
+        f = oracle.forward(x["X"], x["Wg"], x["Wu"], x["Wd"], mode=oracle.EXACT, gate_mul=gm,
+                           down_mul=dm)
+        b = oracle.backward(x["dY"], x["X"], x["Wg"], x["Wu"], x["Wd"], f, mode=oracle.EXACT,
+                            gate_mul=gm, down_mul=dm)
+        _fd_check(x, b, coords_per_tensor=coords, seed=2, gm=gm, dm=dm)
+
+
+def test_accumulated_micro_batches_equal_one_batch(oracle_lib):
+    """Gradient accumulation: the weight gradients of two micro-batches, the
+    second added onto the first, equal those of the concatenated batch."""
+    M, D, H = 12, 16, 24
+    x = _f64_inputs(M, D, H, 16)
+    f = oracle.forward(x["X"], x["Wg"], x["Wu"], x["Wd"], mode=oracle.EXACT, gate_mul=1.3)
+    full = oracle.backward(x["dY"], x["X"], x["Wg"], x["Wu"], x["Wd"], f, mode=oracle.EXACT,
+                           gate_mul=1.3)
+    acc = None
+    for rows in (slice(0, 5), slice(5, M)):
+        part = {k: v[rows] for k, v in f.items()}
+        b = oracle.backward(x["dY"][rows], x["X"][rows], x["Wg"], x["Wu"], x["Wd"], part,
+                            mode=oracle.EXACT, gate_mul=1.3, accumulate=acc)
+        acc = {k: b[k] for k in ("dWg", "dWu", "dWd")}
+    for k in ("dWg", "dWu", "dWd"):
+        assert oracle.rel_frob(acc[k], full[k]) < 1e-13, k
+
+
+def test_accumulation_rounds_once(oracle_lib):
+    """In the rounded program the held gradient and the new sum are added in
+    fp64 and rounded once: tiny contributions below half an ulp of the held
+    value leave it unchanged, as one rounding of the exact sum requires."""
+    M, D, H = 4, 8, 8
+    x = _f64_inputs(M, D, H, 17, dy_std=1e-6)
+    t = {k: torch.from_numpy(v).to(torch.bfloat16) for k, v in x.items()}
+    f = oracle.forward(t["X"], t["Wg"], t["Wu"], t["Wd"])
+    held = {"dWg": np.full((H, D), 1.0), "dWu": np.full((H, D), -1.0),
+            "dWd": np.full((D, H), 2.0)}
+    b = oracle.backward(t["dY"], t["X"], t["Wg"], t["Wu"], t["Wd"], f, accumulate=held)
+    fresh = oracle.backward(t["dY"], t["X"], t["Wg"], t["Wu"], t["Wd"], f)
+    for k in ("dWg", "dWu", "dWd"):
+        assert np.max(np.abs(fresh[k])) < 1e-3           # far below half an ulp of 1.0 in bf16
+        np.testing.assert_array_equal(b[k], held[k])
 
 
 def test_sampled_forms_match_full(oracle_lib):
