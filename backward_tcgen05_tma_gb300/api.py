@@ -44,6 +44,19 @@ class SwigluError(RuntimeError):
         super().__init__("%s: %s (%s)" % (where, STATUS.get(code, code), status_string(code)))
 
 
+class Options(ctypes.Structure):
+    """swiglu_mlp_options: gate/down multipliers and weight-gradient accumulation."""
+    _fields_ = [("gate_multiplier", ctypes.c_float), ("down_multiplier", ctypes.c_float),
+                ("accumulate", ctypes.c_int)]
+
+
+def _opts(gate_mul: float, down_mul: float, accumulate: bool):
+    """NULL for the standard MLP, else a pointer to an Options."""
+    if gate_mul == 1.0 and down_mul == 1.0 and not accumulate:
+        return ctypes.c_void_p(0)
+    return ctypes.byref(Options(float(gate_mul), float(down_mul), 1 if accumulate else 0))
+
+
 def lib() -> ctypes.CDLL:
     """The loaded CUDA library (raises if it has not been built)."""
     global _lib
@@ -74,6 +87,15 @@ def lib() -> ctypes.CDLL:
         L.swiglu_mlp_graph_launch.argtypes = [vp, vp]
         L.swiglu_mlp_graph_destroy.restype = ci
         L.swiglu_mlp_graph_destroy.argtypes = [vp]
+        op = ctypes.c_void_p
+        L.swiglu_mlp_fwd_ex.restype = ci
+        L.swiglu_mlp_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, op, vp, sz, vp]
+        L.swiglu_mlp_fwd_nograd_ex.restype = ci
+        L.swiglu_mlp_fwd_nograd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, op, vp, sz,
+                                               vp]
+        L.swiglu_mlp_bwd_ex.restype = ci
+        L.swiglu_mlp_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, op, vp,
+                                        sz, vp]
         L.swiglu_mlp_bwd.restype = ci
         L.swiglu_mlp_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
         L.swiglu_mlp_query_error.restype = ci
@@ -148,8 +170,10 @@ def _dims(X, Wgu, Wd):
     return M, D, H
 
 
-def swiglu_mlp_fwd(X, Wgu, Wd, out: dict | None = None, ws=None):
-    """Training forward: returns (Y [M,D], saved [M,3H])."""
+def swiglu_mlp_fwd(X, Wgu, Wd, out: dict | None = None, ws=None, gate_mul: float = 1.0,
+                   down_mul: float = 1.0):
+    """Training forward: returns (Y [M,D], saved [M,3H]).  ``gate_mul`` /
+    ``down_mul``: the multiplier variant (swiglu_mlp_fwd_ex)."""
     M, D, H = _dims(X, Wgu, Wd)
     out = out or {}
     Y = out.get("Y")
@@ -157,13 +181,15 @@ def swiglu_mlp_fwd(X, Wgu, Wd, out: dict | None = None, ws=None):
     saved = out.get("saved")
     saved = torch.empty(M, 3 * H, dtype=X.dtype, device=X.device) if saved is None else saved
     ws = workspace(M, D, H, X.dtype, SWIGLU_OP_FWD, X.device) if ws is None else ws
-    _check(lib().swiglu_mlp_fwd(_ptr(X), _ptr(Wgu), _ptr(Wd), _ptr(Y), _ptr(saved), M, D, H,
-                                dtype_code(X.dtype), _ptr(ws), ws.numel(), _stream(X.device)),
+    _check(lib().swiglu_mlp_fwd_ex(_ptr(X), _ptr(Wgu), _ptr(Wd), _ptr(Y), _ptr(saved), M, D, H,
+                                   dtype_code(X.dtype), _opts(gate_mul, down_mul, False),
+                                   _ptr(ws), ws.numel(), _stream(X.device)),
            "swiglu_mlp_fwd")
     return Y, saved
 
 
-def swiglu_mlp_fwd_nograd(X, Wgu, Wd, out: dict | None = None, ws=None):
+def swiglu_mlp_fwd_nograd(X, Wgu, Wd, out: dict | None = None, ws=None, gate_mul: float = 1.0,
+                          down_mul: float = 1.0):
     """Inference forward: returns (Y [M,D], A [M,H]); G and U are never stored."""
     M, D, H = _dims(X, Wgu, Wd)
     out = out or {}
@@ -172,9 +198,10 @@ def swiglu_mlp_fwd_nograd(X, Wgu, Wd, out: dict | None = None, ws=None):
     A = out.get("A")
     A = torch.empty(M, H, dtype=X.dtype, device=X.device) if A is None else A
     ws = workspace(M, D, H, X.dtype, SWIGLU_OP_FWD_NOGRAD, X.device) if ws is None else ws
-    _check(lib().swiglu_mlp_fwd_nograd(_ptr(X), _ptr(Wgu), _ptr(Wd), _ptr(Y), _ptr(A), M, D, H,
-                                       dtype_code(X.dtype), _ptr(ws), ws.numel(),
-                                       _stream(X.device)),
+    _check(lib().swiglu_mlp_fwd_nograd_ex(_ptr(X), _ptr(Wgu), _ptr(Wd), _ptr(Y), _ptr(A), M, D,
+                                          H, dtype_code(X.dtype),
+                                          _opts(gate_mul, down_mul, False), _ptr(ws), ws.numel(),
+                                          _stream(X.device)),
            "swiglu_mlp_fwd_nograd")
     return Y, A
 
@@ -250,9 +277,11 @@ class FwdNogradGraph:
             pass
 
 
-def swiglu_mlp_bwd(dY, X, Wgu, Wd, saved, out: dict | None = None, ws=None):
+def swiglu_mlp_bwd(dY, X, Wgu, Wd, saved, out: dict | None = None, ws=None,
+                   gate_mul: float = 1.0, down_mul: float = 1.0, accumulate: bool = False):
     """Backward: returns (dX [M,D], dWgu [2H,D], dWd [D,H]).  Overwrites the
-    G/U columns of ``saved`` with dG/dU (a second call on it is undefined)."""
+    G/U columns of ``saved`` with dG/dU (a second call on it is undefined).
+    ``accumulate``: add into the dWgu / dWd given in ``out`` (beta = 1)."""
     M, D, H = _dims(X, Wgu, Wd)
     if dY.shape != (M, D) or saved.shape != (M, 3 * H):
         raise ValueError("dY/saved shape mismatch")
@@ -264,9 +293,12 @@ def swiglu_mlp_bwd(dY, X, Wgu, Wd, saved, out: dict | None = None, ws=None):
     dWd = out.get("dWd")
     dWd = torch.empty(D, H, dtype=X.dtype, device=X.device) if dWd is None else dWd
     ws = workspace(M, D, H, X.dtype, SWIGLU_OP_BWD, X.device) if ws is None else ws
-    _check(lib().swiglu_mlp_bwd(_ptr(dY), _ptr(X), _ptr(Wgu), _ptr(Wd), _ptr(saved), _ptr(dX),
-                                _ptr(dWgu), _ptr(dWd), M, D, H, dtype_code(X.dtype), _ptr(ws),
-                                ws.numel(), _stream(X.device)),
+    if accumulate and (out.get("dWgu") is None or out.get("dWd") is None):
+        raise ValueError("accumulate needs the held dWgu and dWd in out")
+    _check(lib().swiglu_mlp_bwd_ex(_ptr(dY), _ptr(X), _ptr(Wgu), _ptr(Wd), _ptr(saved),
+                                   _ptr(dX), _ptr(dWgu), _ptr(dWd), M, D, H,
+                                   dtype_code(X.dtype), _opts(gate_mul, down_mul, accumulate),
+                                   _ptr(ws), ws.numel(), _stream(X.device)),
            "swiglu_mlp_bwd")
     return dX, dWgu, dWd
 

@@ -51,6 +51,7 @@ struct NgArgs {
   int64_t ld_out;
   uint64_t wait_limit_ns;
   int* err;
+  float scale = 1.0f;  // gate/up: gate multiplier (SiLU(scale g) u); down: Y = scale y
 };
 
 template <int NT>
@@ -165,7 +166,7 @@ __device__ __forceinline__ void ng_store_whole(const NgArgs& a, int tile, uint32
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         if (n < a.M) {
-          const float o = silu_f32(v[n]) * ustage[row * NT + n];
+          const float o = silu_f32(a.scale * v[n]) * ustage[row * NT + n];
           if (BF16)
             reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)n * a.ld_out + j] =
                 __float2bfloat16_rn(o);
@@ -183,9 +184,10 @@ __device__ __forceinline__ void ng_store_whole(const NgArgs& a, int tile, uint32
         if (n < a.M) {
           if (BF16)
             reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)n * a.ld_out + d] =
-                __float2bfloat16_rn(v[n]);
+                __float2bfloat16_rn(a.scale * v[n]);
           else
-            reinterpret_cast<__half*>(a.out)[(int64_t)n * a.ld_out + d] = __float2half_rn(v[n]);
+            reinterpret_cast<__half*>(a.out)[(int64_t)n * a.ld_out + d] =
+                __float2half_rn(a.scale * v[n]);
         }
       }
     }
@@ -260,7 +262,7 @@ __device__ __forceinline__ void ng_reduce_store(const NgArgs& a, int tile, int n
       for (int q = 0; q < NT / 2; ++q) {
         const int m = h * (NT / 2) + q;
         if (m < a.M) {
-          const float v = silu_f32(g[q]) * uu[q];
+          const float v = silu_f32(a.scale * g[q]) * uu[q];
           if (BF16)
             reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)m * a.ld_out + j] =
                 __float2bfloat16_rn(v);
@@ -300,9 +302,10 @@ __device__ __forceinline__ void ng_reduce_store(const NgArgs& a, int tile, int n
         if (q < a.M) {
           if (BF16)
             reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)q * a.ld_out + d] =
-                __float2bfloat16_rn(y[q]);
+                __float2bfloat16_rn(a.scale * y[q]);
           else
-            reinterpret_cast<__half*>(a.out)[(int64_t)q * a.ld_out + d] = __float2half_rn(y[q]);
+            reinterpret_cast<__half*>(a.out)[(int64_t)q * a.ld_out + d] =
+                __float2half_rn(a.scale * y[q]);
         }
       }
     }

@@ -29,20 +29,26 @@ struct SimtOperand {
 struct SimtEpiStore {
   float* out;
   int64_t ld;
+  float scale = 1.0f;   // out = scale * acc ...
+  int accumulate = 0;   // ... or, if nonzero, out + scale * acc
   __device__ __forceinline__ void apply(int m, int n, float acc, float) const {
-    out[(int64_t)m * ld + n] = acc;
+    float* o = out + (int64_t)m * ld + n;
+    *o = accumulate ? *o + scale * acc : scale * acc;
   }
 };
 
-// Gate/up: acc = g, acc2 = u for hidden unit n.  Stores G, U (if g != null)
-// and A = SiLU(g) * u, SiLU(g) = g / (1 + e^-g) with IEEE expf and division.
+// Gate/up: acc = X Wg^T, acc2 = u for hidden unit n; g = gate_mul * acc.
+// Stores G = g, U (if g != null) and A = SiLU(g) * u, SiLU(g) = g / (1 + e^-g)
+// with IEEE expf and division.
 struct SimtEpiSwiGLU {
   float* g;
   float* u;
   int64_t ld_gu;
   float* a;
   int64_t ld_a;
-  __device__ __forceinline__ void apply(int m, int n, float gv, float uv) const {
+  float gate_mul = 1.0f;
+  __device__ __forceinline__ void apply(int m, int n, float acc, float uv) const {
+    const float gv = gate_mul * acc;
     if (g != nullptr) {
       g[(int64_t)m * ld_gu + n] = gv;
       u[(int64_t)m * ld_gu + n] = uv;
@@ -51,18 +57,21 @@ struct SimtEpiSwiGLU {
   }
 };
 
-// Backward: acc = dA for hidden unit n; reads the stored G, U and overwrites
-// them with dG = dA * U * SiLU'(G), dU = dA * SiLU(G).
+// Backward: acc = dY Wd for hidden unit n, dA = down_mul * acc; reads the
+// stored G (= gate_mul X Wg^T), U and overwrites them with
+// dG = dA * U * SiLU'(G) * gate_mul, dU = dA * SiLU(G).
 struct SimtEpiDSwiGLU {
   float* g;
   float* u;
   int64_t ld;
-  __device__ __forceinline__ void apply(int m, int n, float da, float) const {
+  float gate_mul = 1.0f, down_mul = 1.0f;
+  __device__ __forceinline__ void apply(int m, int n, float acc, float) const {
     const int64_t o = (int64_t)m * ld + n;
+    const float da = down_mul * acc;
     const float gv = g[o], uv = u[o];
     const float s = 1.0f / (1.0f + expf(-gv));
     u[o] = da * (gv * s);
-    g[o] = da * uv * (s * (1.0f + gv * (1.0f - s)));
+    g[o] = da * uv * (s * (1.0f + gv * (1.0f - s)) * gate_mul);
   }
 };
 

@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -37,6 +38,13 @@ constexpr int TC_BN = 256;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 
 swiglu_status cuda_status(cudaError_t e);
+
+// The multiplier / accumulation options of the _ex entry points (see the
+// header); {1, 1, 0} is the standard MLP with gradients overwritten.
+struct Opts {
+  float gm = 1.0f, dm = 1.0f;
+  int acc = 0;
+};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_last_launches{0};
 std::atomic<int> g_cta_pairs{1};  // SM pairs (cta_group::2): 0 never, 1 by size, 2 always
@@ -536,7 +544,7 @@ cudaError_t launch_ng(int kid, const CUtensorMap& tw, const CUtensorMap& tx, NgA
 template <int NT, bool BF16>
 swiglu_status ng_forward_nt(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
                             int64_t M, int64_t D, int64_t H, const NgPlan& p, char* ws,
-                            cudaStream_t st) {
+                            const Opts& o, cudaStream_t st) {
   int* err = reinterpret_cast<int*>(ws);
   int* counters = reinterpret_cast<int*>(ws + WS_HEADER);
   float* part = reinterpret_cast<float*>(ws + WS_HEADER + p.counter_bytes);
@@ -546,12 +554,14 @@ swiglu_status ng_forward_nt(const void* X, const void* Wgu, const void* Wd, void
     return SWIGLU_ERR_CUDA;
   NgArgs a1{(int)M, (int)H, p.kb1, p.t1, 0, 0, part, counters, counters + p.t1, p.t2, 1, 0, 0,
             A, H, wl, err};
+  a1.scale = o.gm;
   if (launch_ng<NT, true, BF16>(K_NG_GATE_UP, tw, tx, a1, st) != cudaSuccess)
     return SWIGLU_ERR_CUDA;
   if (!map_kmajor(&tw, BF16, Wd, H, D, H, 128) || !map_kmajor(&tx, BF16, A, H, M, H, NT))
     return SWIGLU_ERR_CUDA;
   NgArgs a2{(int)M, (int)D, p.kb2, p.t2, 0, 0, part, counters + p.t1, counters, p.t1, 0, 1, 0,
             Y, D, wl, err};
+  a2.scale = o.dm;
   return cuda_status(launch_ng<NT, false, BF16>(K_NG_DOWN, tw, tx, a2, st));
 }
 
@@ -565,7 +575,7 @@ constexpr size_t NG_NEXT_OFFSET = 192;  // the fused kernel's work-queue counter
 template <int NT, bool BF16>
 swiglu_status ng_forward_fused(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
                                int64_t M, int64_t D, int64_t H, const NgPlan& p, char* ws,
-                               cudaStream_t st) {
+                               const Opts& o, cudaStream_t st) {
   auto kern = ng_fused_kernel<NT, BF16>;
   constexpr int smem = NgDynSmem<NT>::DYN_BYTES;
   {
@@ -605,6 +615,8 @@ swiglu_status ng_forward_fused(const void* X, const void* Wgu, const void* Wd, v
                    A, H, wl, err};
   f.ph[1] = NgArgs{(int)M, (int)D, p.kb2, p.t2, 0, 0, part1, counters + p.t1, nullptr, 0, 0, 0,
                    0, Y, D, wl, err};
+  f.ph[0].scale = o.gm;
+  f.ph[1].scale = o.dm;
   ProfScope prof(K_NG_FUSED, st);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)d.grid);
@@ -623,23 +635,23 @@ swiglu_status ng_forward_fused(const void* X, const void* Wgu, const void* Wd, v
 template <int NT, bool BF16>
 swiglu_status ng_forward_t(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
                            int64_t M, int64_t D, int64_t H, const NgPlan& p, char* ws,
-                           size_t ws_cap, cudaStream_t st) {
+                           size_t ws_cap, const Opts& o, cudaStream_t st) {
   const int mode = g_ng_fused.load();
   if ((mode == 2 || (mode == 1 && NT == 64)) && ng_fused_bytes(p) <= ws_cap)
-    return ng_forward_fused<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, st);
+    return ng_forward_fused<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, o, st);
   if (ng_two_bytes(p) > ws_cap) return SWIGLU_ERR_UNSUPPORTED;
-  return ng_forward_nt<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, st);
+  return ng_forward_nt<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, o, st);
 }
 
 template <bool BF16>
 swiglu_status ng_forward(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
                          int64_t M, int64_t D, int64_t H, char* ws, size_t ws_cap,
-                         cudaStream_t st) {
+                         const Opts& o, cudaStream_t st) {
   const NgPlan p = ng_plan(M, D, H);
   switch (p.NT) {
-    case 16: return ng_forward_t<16, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, st);
-    case 32: return ng_forward_t<32, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, st);
-    default: return ng_forward_t<64, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, st);
+    case 16: return ng_forward_t<16, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, o, st);
+    case 32: return ng_forward_t<32, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, o, st);
+    default: return ng_forward_t<64, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, o, st);
   }
 }
 
@@ -713,13 +725,28 @@ swiglu_status cuda_status(cudaError_t e) {
   return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 
+// Reads and checks the options of an _ex call (NULL: the defaults).
+swiglu_status read_opts(const swiglu_mlp_options* in, bool backward, Opts* out) {
+  Opts o;
+  if (in != nullptr) {
+    if (!std::isfinite(in->gate_multiplier) || !std::isfinite(in->down_multiplier))
+      return SWIGLU_ERR_INVALID_ARG;
+    if (in->accumulate != 0 && (in->accumulate != 1 || !backward)) return SWIGLU_ERR_INVALID_ARG;
+    o.gm = in->gate_multiplier;
+    o.dm = in->down_multiplier;
+    o.acc = in->accumulate;
+  }
+  *out = o;
+  return SWIGLU_OK;
+}
+
 // ---------------------------------------------------------------------------
 // tensor-core (bf16 / fp16) paths
 // ---------------------------------------------------------------------------
 template <bool BF16>
 swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y, void* G,
                          void* U, int64_t ld_gu, void* A, int64_t ld_a, int64_t M, int64_t D,
-                         int64_t H, int* err, cudaStream_t st) {
+                         int64_t H, int* err, const Opts& o, cudaStream_t st) {
   CUtensorMap tx, tw, ta, twd;
   // gate/up + SwiGLU: C[m, j | H + j], N counts hidden units, BN/2 per tile;
   // on a pair each CTA brings one of Wg, Wu
@@ -728,7 +755,7 @@ swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y
       !encode_gateup(&tw, BF16, Wgu, D, H, TC_BN / 2, pairs1 ? 1 : 2))
     return SWIGLU_ERR_CUDA;
   TcShape s1 = make_shape(M, H, D, TC_BN / 2, err, pairs1);
-  EpiSwiGLU::Params p1{G, U, ld_gu, A, ld_a};
+  EpiSwiGLU::Params p1{G, U, ld_gu, A, ld_a, o.gm};
   cudaError_t e = launch_gemm<LOAD_KMAJOR, LOAD_GATEUP, BF16, EpiSwiGLU>(
       pairs1, G != nullptr ? K_GATE_UP : K_GATE_UP_NOGRAD, tx, tw, s1, p1, st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
@@ -739,7 +766,7 @@ swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y
       !map_kmajor(&twd, BF16, Wd, H, D, H, pairs2 ? 128 : TC_BN))
     return SWIGLU_ERR_CUDA;
   TcShape s2 = make_shape(M, D, H, TC_BN, err, pairs2);
-  EpiStore::Params p2{Y, D};
+  EpiStore::Params p2{Y, D, o.dm, 0};
   return cuda_status(launch_gemm<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore>(
       pairs2, G != nullptr ? K_DOWN : K_DOWN_NOGRAD, ta, twd, s2, p2, st));
 }
@@ -747,7 +774,7 @@ swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y
 template <bool BF16>
 swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const void* Wd,
                           void* saved, void* dX, void* dWgu, void* dWd, int64_t M, int64_t D,
-                          int64_t H, int* err, cudaStream_t st) {
+                          int64_t H, int* err, const Opts& o, cudaStream_t st) {
   const int64_t ld = 3 * H;
   char* sv = static_cast<char*>(saved);
   void* G = sv;
@@ -761,7 +788,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   {
     const bool pairs = use_pairs(D, H, TC_BN, M);
     TcShape s = make_shape(D, H, M, TC_BN, err, pairs);
-    EpiStore::Params p{dWd, H};
+    EpiStore::Params p{dWd, H, o.dm, o.acc};
     e = launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWD, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
@@ -771,7 +798,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   {
     const bool pairs = use_pairs(M, H, TC_BN, D);
     TcShape s = make_shape(M, H, D, TC_BN, err, pairs);
-    EpiDSwiGLU::Params p{G, U, ld};
+    EpiDSwiGLU::Params p{G, U, ld, o.gm, o.dm};
     e = launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLU>(pairs, K_DGU, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
@@ -781,7 +808,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   {
     const bool pairs = use_pairs(2 * H, D, TC_BN, M);
     TcShape s = make_shape(2 * H, D, M, TC_BN, err, pairs);
-    EpiStore::Params p{dWgu, D};
+    EpiStore::Params p{dWgu, D, 1.0f, o.acc};
     e = launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWGU, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
@@ -791,7 +818,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   {
     const bool pairs = use_pairs(M, D, TC_BN, 2 * H);
     TcShape s = make_shape(M, D, 2 * H, TC_BN, err, pairs);
-    EpiStore::Params p{dX, D};
+    EpiStore::Params p{dX, D, 1.0f, 0};
     e = launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DX, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
@@ -803,17 +830,17 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
 // ---------------------------------------------------------------------------
 swiglu_status simt_forward(const float* X, const float* Wgu, const float* Wd, float* Y, float* G,
                            float* U, int64_t ld_gu, float* A, int64_t ld_a, int64_t M, int64_t D,
-                           int64_t H, cudaStream_t st) {
+                           int64_t H, const Opts& o, cudaStream_t st) {
   SimtOperand x{X, D, 1}, wg{Wgu, D, 1}, wu{Wgu + H * D, D, 1};
-  cudaError_t e = launch_simt<true>(K_SIMT_GATE_UP, x, wg, wu, M, H, D, SimtEpiSwiGLU{G, U, ld_gu, A, ld_a}, st);
+  cudaError_t e = launch_simt<true>(K_SIMT_GATE_UP, x, wg, wu, M, H, D, SimtEpiSwiGLU{G, U, ld_gu, A, ld_a, o.gm}, st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   SimtOperand a{A, ld_a, 1}, wd{Wd, H, 1};
-  return cuda_status(launch_simt<false>(K_SIMT_DOWN, a, wd, wd, M, D, H, SimtEpiStore{Y, D}, st));
+  return cuda_status(launch_simt<false>(K_SIMT_DOWN, a, wd, wd, M, D, H, SimtEpiStore{Y, D, o.dm, 0}, st));
 }
 
 swiglu_status simt_backward(const float* dY, const float* X, const float* Wgu, const float* Wd,
                             float* saved, float* dX, float* dWgu, float* dWd, int64_t M,
-                            int64_t D, int64_t H, cudaStream_t st) {
+                            int64_t D, int64_t H, const Opts& o, cudaStream_t st) {
   const int64_t ld = 3 * H;
   float* G = saved;
   float* U = saved + H;
@@ -821,19 +848,19 @@ swiglu_status simt_backward(const float* dY, const float* X, const float* Wgu, c
   cudaError_t e;
   // dA = dY Wd: A(m, d) = dY[m, d]; B(j, d) = Wd[d, j]
   e = launch_simt<false>(K_SIMT_DGU, SimtOperand{dY, D, 1}, SimtOperand{Wd, 1, H}, SimtOperand{Wd, 1, H}, M,
-                         H, D, SimtEpiDSwiGLU{G, U, ld}, st);
+                         H, D, SimtEpiDSwiGLU{G, U, ld, o.gm, o.dm}, st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   // dWd[d, j] = sum_m dY[m, d] A[m, j]
   e = launch_simt<false>(K_SIMT_DWD, SimtOperand{dY, 1, D}, SimtOperand{A, 1, ld}, SimtOperand{A, 1, ld}, D,
-                         H, M, SimtEpiStore{dWd, H}, st);
+                         H, M, SimtEpiStore{dWd, H, o.dm, o.acc}, st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   // dWgu[j', d] = sum_m dGU[m, j'] X[m, d]
   e = launch_simt<false>(K_SIMT_DWGU, SimtOperand{G, 1, ld}, SimtOperand{X, 1, D}, SimtOperand{X, 1, D}, 2 * H,
-                         D, M, SimtEpiStore{dWgu, D}, st);
+                         D, M, SimtEpiStore{dWgu, D, 1.0f, o.acc}, st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   // dX[m, d] = sum_j' dGU[m, j'] Wgu[j', d]
   e = launch_simt<false>(K_SIMT_DX, SimtOperand{G, ld, 1}, SimtOperand{Wgu, 1, D}, SimtOperand{Wgu, 1, D}, M,
-                         D, 2 * H, SimtEpiStore{dX, D}, st);
+                         D, 2 * H, SimtEpiStore{dX, D, 1.0f, 0}, st);
   return cuda_status(e);
 }
 
@@ -863,11 +890,15 @@ size_t swiglu_mlp_workspace_bytes(int64_t M, int64_t D, int64_t H, swiglu_dtype 
   return WS_HEADER;
 }
 
-swiglu_status swiglu_mlp_fwd(const void* X, const void* Wgu, const void* Wd, void* Y, void* saved,
-                             int64_t M, int64_t D, int64_t H, swiglu_dtype dtype, void* ws,
-                             size_t ws_bytes, void* stream) {
+swiglu_status swiglu_mlp_fwd_ex(const void* X, const void* Wgu, const void* Wd, void* Y,
+                                void* saved, int64_t M, int64_t D, int64_t H,
+                                swiglu_dtype dtype, const swiglu_mlp_options* options,
+                                void* ws, size_t ws_bytes, void* stream) {
   g_last_launches.store(0);
-  swiglu_status st = check_common(M, D, H, dtype, ws, ws_bytes, SWIGLU_OP_FWD);
+  Opts o;
+  swiglu_status st = read_opts(options, false, &o);
+  if (st != SWIGLU_OK) return st;
+  st = check_common(M, D, H, dtype, ws, ws_bytes, SWIGLU_OP_FWD);
   if (st != SWIGLU_OK) return st;
   if (M == 0) return SWIGLU_OK;
   if ((st = check_ptrs({X, Wgu, Wd, Y, saved})) != SWIGLU_OK) return st;
@@ -881,40 +912,58 @@ swiglu_status swiglu_mlp_fwd(const void* X, const void* Wgu, const void* Wd, voi
   void* A = sv + 2 * H * e;
   switch (dtype) {
     case SWIGLU_BF16:
-      return tc_forward<true>(X, Wgu, Wd, Y, G, U, 3 * H, A, 3 * H, M, D, H, err, s);
+      return tc_forward<true>(X, Wgu, Wd, Y, G, U, 3 * H, A, 3 * H, M, D, H, err, o, s);
     case SWIGLU_F16:
-      return tc_forward<false>(X, Wgu, Wd, Y, G, U, 3 * H, A, 3 * H, M, D, H, err, s);
+      return tc_forward<false>(X, Wgu, Wd, Y, G, U, 3 * H, A, 3 * H, M, D, H, err, o, s);
     default:
       return simt_forward((const float*)X, (const float*)Wgu, (const float*)Wd, (float*)Y,
-                          (float*)G, (float*)U, 3 * H, (float*)A, 3 * H, M, D, H, s);
+                          (float*)G, (float*)U, 3 * H, (float*)A, 3 * H, M, D, H, o, s);
   }
 }
 
-swiglu_status swiglu_mlp_fwd_nograd(const void* X, const void* Wgu, const void* Wd, void* Y,
-                                    void* A, int64_t M, int64_t D, int64_t H, swiglu_dtype dtype,
-                                    void* ws, size_t ws_bytes, void* stream) {
+swiglu_status swiglu_mlp_fwd(const void* X, const void* Wgu, const void* Wd, void* Y, void* saved,
+                             int64_t M, int64_t D, int64_t H, swiglu_dtype dtype, void* ws,
+                             size_t ws_bytes, void* stream) {
+  return swiglu_mlp_fwd_ex(X, Wgu, Wd, Y, saved, M, D, H, dtype, nullptr, ws, ws_bytes, stream);
+}
+
+swiglu_status swiglu_mlp_fwd_nograd_ex(const void* X, const void* Wgu, const void* Wd, void* Y,
+                                       void* A, int64_t M, int64_t D, int64_t H,
+                                       swiglu_dtype dtype, const swiglu_mlp_options* options,
+                                       void* ws, size_t ws_bytes, void* stream) {
   g_last_launches.store(0);
-  swiglu_status st = check_common(M, D, H, dtype, ws, ws_bytes, SWIGLU_OP_FWD_NOGRAD);
+  Opts o;
+  swiglu_status st = read_opts(options, false, &o);
+  if (st != SWIGLU_OK) return st;
+  st = check_common(M, D, H, dtype, ws, ws_bytes, SWIGLU_OP_FWD_NOGRAD);
   if (st != SWIGLU_OK) return st;
   if (M == 0) return SWIGLU_OK;
   if ((st = check_ptrs({X, Wgu, Wd, Y, A})) != SWIGLU_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (ng_eligible(M, D, H, dtype)) {
     char* w = static_cast<char*>(ws);
-    return dtype == SWIGLU_BF16 ? ng_forward<true>(X, Wgu, Wd, Y, A, M, D, H, w, ws_bytes, s)
-                                : ng_forward<false>(X, Wgu, Wd, Y, A, M, D, H, w, ws_bytes, s);
+    return dtype == SWIGLU_BF16
+               ? ng_forward<true>(X, Wgu, Wd, Y, A, M, D, H, w, ws_bytes, o, s)
+               : ng_forward<false>(X, Wgu, Wd, Y, A, M, D, H, w, ws_bytes, o, s);
   }
   int* err = static_cast<int*>(ws);
   if (cudaMemsetAsync(err, 0, ws_clear_bytes(dtype), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
   switch (dtype) {
     case SWIGLU_BF16:
-      return tc_forward<true>(X, Wgu, Wd, Y, nullptr, nullptr, 0, A, H, M, D, H, err, s);
+      return tc_forward<true>(X, Wgu, Wd, Y, nullptr, nullptr, 0, A, H, M, D, H, err, o, s);
     case SWIGLU_F16:
-      return tc_forward<false>(X, Wgu, Wd, Y, nullptr, nullptr, 0, A, H, M, D, H, err, s);
+      return tc_forward<false>(X, Wgu, Wd, Y, nullptr, nullptr, 0, A, H, M, D, H, err, o, s);
     default:
       return simt_forward((const float*)X, (const float*)Wgu, (const float*)Wd, (float*)Y,
-                          nullptr, nullptr, 0, (float*)A, H, M, D, H, s);
+                          nullptr, nullptr, 0, (float*)A, H, M, D, H, o, s);
   }
+}
+
+swiglu_status swiglu_mlp_fwd_nograd(const void* X, const void* Wgu, const void* Wd, void* Y,
+                                    void* A, int64_t M, int64_t D, int64_t H, swiglu_dtype dtype,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  return swiglu_mlp_fwd_nograd_ex(X, Wgu, Wd, Y, A, M, D, H, dtype, nullptr, ws, ws_bytes,
+                                  stream);
 }
 
 swiglu_status swiglu_mlp_fwd_nograd_noalloc(const void* X, const void* Wgu, const void* Wd,
@@ -940,16 +989,20 @@ swiglu_status swiglu_mlp_fwd_nograd_noalloc(const void* X, const void* Wgu, cons
     return SWIGLU_ERR_CUDA;
   char* w = static_cast<char*>(scratch);
   return dtype == SWIGLU_BF16
-             ? ng_forward<true>(X, Wgu, Wd, Y, A, M, D, H, w, NOALLOC_SCRATCH_BYTES, s)
-             : ng_forward<false>(X, Wgu, Wd, Y, A, M, D, H, w, NOALLOC_SCRATCH_BYTES, s);
+             ? ng_forward<true>(X, Wgu, Wd, Y, A, M, D, H, w, NOALLOC_SCRATCH_BYTES, Opts{}, s)
+             : ng_forward<false>(X, Wgu, Wd, Y, A, M, D, H, w, NOALLOC_SCRATCH_BYTES, Opts{}, s);
 }
 
-swiglu_status swiglu_mlp_bwd(const void* dY, const void* X, const void* Wgu, const void* Wd,
-                             void* saved, void* dX, void* dWgu, void* dWd, int64_t M, int64_t D,
-                             int64_t H, swiglu_dtype dtype, void* ws, size_t ws_bytes,
-                             void* stream) {
+swiglu_status swiglu_mlp_bwd_ex(const void* dY, const void* X, const void* Wgu, const void* Wd,
+                                void* saved, void* dX, void* dWgu, void* dWd, int64_t M,
+                                int64_t D, int64_t H, swiglu_dtype dtype,
+                                const swiglu_mlp_options* options, void* ws, size_t ws_bytes,
+                                void* stream) {
   g_last_launches.store(0);
-  swiglu_status st = check_common(M, D, H, dtype, ws, ws_bytes, SWIGLU_OP_BWD);
+  Opts o;
+  swiglu_status st = read_opts(options, true, &o);
+  if (st != SWIGLU_OK) return st;
+  st = check_common(M, D, H, dtype, ws, ws_bytes, SWIGLU_OP_BWD);
   if (st != SWIGLU_OK) return st;
   if (M == 0) return SWIGLU_OK;  // gradients of an empty batch: nothing is written
   if ((st = check_ptrs({dY, X, Wgu, Wd, saved, dX, dWgu, dWd})) != SWIGLU_OK) return st;
@@ -958,14 +1011,22 @@ swiglu_status swiglu_mlp_bwd(const void* dY, const void* X, const void* Wgu, con
   if (cudaMemsetAsync(err, 0, ws_clear_bytes(dtype), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
   switch (dtype) {
     case SWIGLU_BF16:
-      return tc_backward<true>(dY, X, Wgu, Wd, saved, dX, dWgu, dWd, M, D, H, err, s);
+      return tc_backward<true>(dY, X, Wgu, Wd, saved, dX, dWgu, dWd, M, D, H, err, o, s);
     case SWIGLU_F16:
-      return tc_backward<false>(dY, X, Wgu, Wd, saved, dX, dWgu, dWd, M, D, H, err, s);
+      return tc_backward<false>(dY, X, Wgu, Wd, saved, dX, dWgu, dWd, M, D, H, err, o, s);
     default:
       return simt_backward((const float*)dY, (const float*)X, (const float*)Wgu,
                            (const float*)Wd, (float*)saved, (float*)dX, (float*)dWgu,
-                           (float*)dWd, M, D, H, s);
+                           (float*)dWd, M, D, H, o, s);
   }
+}
+
+swiglu_status swiglu_mlp_bwd(const void* dY, const void* X, const void* Wgu, const void* Wd,
+                             void* saved, void* dX, void* dWgu, void* dWd, int64_t M, int64_t D,
+                             int64_t H, swiglu_dtype dtype, void* ws, size_t ws_bytes,
+                             void* stream) {
+  return swiglu_mlp_bwd_ex(dY, X, Wgu, Wd, saved, dX, dWgu, dWd, M, D, H, dtype, nullptr, ws,
+                           ws_bytes, stream);
 }
 
 struct swiglu_mlp_graph {

@@ -237,7 +237,9 @@ __device__ __forceinline__ float silu_f32(float g) { return g * sigmoid_f32(g); 
 struct EpiStore {
   struct Params {
     void* out;
-    int64_t ld;  // elements
+    int64_t ld;          // elements
+    float scale;         // out = rnd(scale * acc) ...
+    int accumulate;      // ... or, if nonzero, rnd(out + scale * acc) (one rounding)
   };
   template <int BN, bool BF16>
   static __device__ __forceinline__ void run(const Params& p, const TcShape& s, uint32_t tacc,
@@ -249,30 +251,45 @@ struct EpiStore {
     const int n0 = nt * BN;
 #pragma unroll 1
     for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
+      const int nc = n0 + c * 32;
+      auto rows = [&](int rr) -> uint8_t* {
+        const int m = mw + rr;
+        return m < s.M ? reinterpret_cast<uint8_t*>(reinterpret_cast<T*>(p.out) +
+                                                    (int64_t)m * p.ld + nc)
+                       : nullptr;
+      };
+      auto ok = [&](int q) { return nc + q * 8 + 8 <= s.N; };
+      uint4 old[4];
+      if (p.accumulate) {
+        uint4 w[4];
+        warp_load_issue(w, lane, rows, ok);
+        warp_load_finish(buf, w, lane, old);
+      }
       uint32_t r[32];
       tmem_ld_32x32b_x32(tacc + c * 32, r);
       tmem_ld_wait();
       uint32_t v[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = P::two(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-      const int nc = n0 + c * 32;
-      warp_store_tile(
-          buf, v, lane,
-          [&](int rr) -> uint8_t* {
-            const int m = mw + rr;
-            return m < s.M ? reinterpret_cast<uint8_t*>(reinterpret_cast<T*>(p.out) +
-                                                        (int64_t)m * p.ld + nc)
-                           : nullptr;
-          },
-          [&](int q) { return nc + q * 8 + 8 <= s.N; });
+      for (int i = 0; i < 16; ++i) {
+        float a0 = p.scale * __uint_as_float(r[2 * i]);
+        float a1 = p.scale * __uint_as_float(r[2 * i + 1]);
+        if (p.accumulate) {
+          const float2 o = P::unpack((&old[i >> 2].x)[i & 3]);
+          a0 += o.x;
+          a1 += o.y;
+        }
+        v[i] = P::two(a0, a1);
+      }
+      warp_store_tile(buf, v, lane, rows, ok);
     }
   }
 };
 
-// Gate/up epilogue: accumulator columns [0, BN/2) hold G for hidden units
-// j0 .. j0 + BN/2 - 1 and [BN/2, BN) hold U for the same units.  Stores
-// rnd(G), rnd(U) (training) and A = rnd(SiLU(G) * U) from the unrounded fp32
-// values.  With g == nullptr only A is written (no-grad).
+// Gate/up epilogue: accumulator columns [0, BN/2) hold X Wg^T for hidden
+// units j0 .. j0 + BN/2 - 1 and [BN/2, BN) hold U for the same units.  With
+// G = gate_mul * (X Wg^T) (1 for the standard MLP) it stores rnd(G), rnd(U)
+// (training) and A = rnd(SiLU(G) * U) from the unrounded fp32 values.  With
+// g == nullptr only A is written (no-grad).
 struct EpiSwiGLU {
   struct Params {
     void* g;       // G base ([M, ld_gu]); U at u
@@ -280,6 +297,7 @@ struct EpiSwiGLU {
     int64_t ld_gu;
     void* a;       // A base
     int64_t ld_a;
+    float gate_mul;
   };
   template <int BN, bool BF16>
   static __device__ __forceinline__ void run(const Params& p, const TcShape& s, uint32_t tacc,
@@ -300,7 +318,8 @@ struct EpiSwiGLU {
       uint32_t va[16], vg[16], vu[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float g0 = __uint_as_float(rg[2 * i]), g1 = __uint_as_float(rg[2 * i + 1]);
+        const float g0 = p.gate_mul * __uint_as_float(rg[2 * i]);
+        const float g1 = p.gate_mul * __uint_as_float(rg[2 * i + 1]);
         const float u0 = __uint_as_float(ru[2 * i]), u1 = __uint_as_float(ru[2 * i + 1]);
         va[i] = P::two(silu_f32(g0) * u0, silu_f32(g1) * u1);
         vg[i] = P::two(g0, g1);
@@ -324,15 +343,18 @@ struct EpiSwiGLU {
   }
 };
 
-// Backward SwiGLU epilogue: the accumulator is dA = dY Wd for hidden units
-// j0 .. j0 + BN - 1 (never stored).  Reads the stored G, U, writes
-//   dU = rnd(dA * SiLU(G)),  dG = rnd(dA * U * SiLU'(G))
-// over them in place, SiLU'(g) = s (1 + g (1 - s)), s = 1 / (1 + e^-g).
+// Backward SwiGLU epilogue: the accumulator is dY Wd for hidden units
+// j0 .. j0 + BN - 1; dA = down_mul * (dY Wd) is never stored.  Reads the
+// stored G (= gate_mul X Wg^T), U, writes
+//   dU = rnd(dA * SiLU(G)),  dG = rnd(dA * U * SiLU'(G) * gate_mul)
+// over them in place, SiLU'(g) = s (1 + g (1 - s)), s = 1 / (1 + e^-g); dG
+// is the gradient with respect to X Wg^T.
 struct EpiDSwiGLU {
   struct Params {
     void* g;  // G (becomes dG); U (becomes dU) at u
     void* u;
     int64_t ld;
+    float gate_mul, down_mul;
   };
   template <int BN, bool BF16>
   static __device__ __forceinline__ void run(const Params& p, const TcShape& s, uint32_t tacc,
@@ -383,12 +405,12 @@ struct EpiDSwiGLU {
         for (int e = 0; e < 4; ++e) {
           const float2 g = P::unpack(pg[e]);
           const float2 u = P::unpack(pu[e]);
-          const float da0 = __uint_as_float(r[g8 * 8 + 2 * e]);
-          const float da1 = __uint_as_float(r[g8 * 8 + 2 * e + 1]);
+          const float da0 = p.down_mul * __uint_as_float(r[g8 * 8 + 2 * e]);
+          const float da1 = p.down_mul * __uint_as_float(r[g8 * 8 + 2 * e + 1]);
           const float s0 = sigmoid_f32(g.x);
           const float s1 = sigmoid_f32(g.y);
-          const float ds0 = s0 * (1.0f + g.x * (1.0f - s0));
-          const float ds1 = s1 * (1.0f + g.y * (1.0f - s1));
+          const float ds0 = s0 * (1.0f + g.x * (1.0f - s0)) * p.gate_mul;
+          const float ds1 = s1 * (1.0f + g.y * (1.0f - s1)) * p.gate_mul;
           odu[g8 * 4 + e] = P::two(da0 * (g.x * s0), da1 * (g.y * s1));
           odg[g8 * 4 + e] = P::two(da0 * u.x * ds0, da1 * u.y * ds1);
         }

@@ -23,16 +23,18 @@ from . import api
 
 
 class SwiGLUMLPFunction(torch.autograd.Function):
-    """Y = (SiLU(X Wg^T) * (X Wu^T)) Wd^T with Wgu = [Wg; Wu] ([2H, D])."""
+    """Y = md (SiLU(mg X Wg^T) * (X Wu^T)) Wd^T with Wgu = [Wg; Wu] ([2H, D]);
+    the gate/down multipliers mg, md are 1 for the standard MLP."""
 
     @staticmethod
-    def forward(ctx, X, Wgu, Wd):
+    def forward(ctx, X, Wgu, Wd, gate_mul=1.0, down_mul=1.0):
         D = X.shape[-1]
         lead = X.shape[:-1]
         X2 = X.reshape(-1, D).contiguous()
-        Y, saved = api.swiglu_mlp_fwd(X2, Wgu, Wd)
+        Y, saved = api.swiglu_mlp_fwd(X2, Wgu, Wd, gate_mul=gate_mul, down_mul=down_mul)
         ctx.save_for_backward(X2, Wgu, Wd, saved)
         ctx.lead = lead
+        ctx.muls = (gate_mul, down_mul)
         ctx.consumed = False
         return Y.reshape(*lead, D)
 
@@ -46,17 +48,19 @@ class SwiGLUMLPFunction(torch.autograd.Function):
         X2, Wgu, Wd, saved = ctx.saved_tensors
         D = X2.shape[1]
         dY2 = dY.reshape(-1, D).to(X2.dtype).contiguous()
-        dX, dWgu, dWd = api.swiglu_mlp_bwd(dY2, X2, Wgu, Wd, saved)
-        return dX.reshape(*ctx.lead, D), dWgu, dWd
+        dX, dWgu, dWd = api.swiglu_mlp_bwd(dY2, X2, Wgu, Wd, saved, gate_mul=ctx.muls[0],
+                                           down_mul=ctx.muls[1])
+        return dX.reshape(*ctx.lead, D), dWgu, dWd, None, None
 
 
-def swiglu_mlp(X, Wgu, Wd):
+def swiglu_mlp(X, Wgu, Wd, gate_mul: float = 1.0, down_mul: float = 1.0):
     """Functional form: autograd-aware when any input requires grad, otherwise
     the no-grad path (A and Y only, no G/U saved)."""
     if torch.is_grad_enabled() and (X.requires_grad or Wgu.requires_grad or Wd.requires_grad):
-        return SwiGLUMLPFunction.apply(X, Wgu, Wd)
+        return SwiGLUMLPFunction.apply(X, Wgu, Wd, float(gate_mul), float(down_mul))
     D = X.shape[-1]
-    Y, _ = api.swiglu_mlp_fwd_nograd(X.reshape(-1, D).contiguous(), Wgu, Wd)
+    Y, _ = api.swiglu_mlp_fwd_nograd(X.reshape(-1, D).contiguous(), Wgu, Wd, gate_mul=gate_mul,
+                                     down_mul=down_mul)
     return Y.reshape(*X.shape[:-1], D)
 
 
@@ -65,12 +69,23 @@ class SwiGLUMLP(torch.nn.Module):
 
     The gate and up projection weights live in one parameter ``gate_up_weight``
     ([2H, D]: gate rows then up rows, as the kernels read them); ``gate_weight``
-    and ``up_weight`` are views of it.  ``down_weight`` is [D, H].
+    and ``up_weight`` are views of it.  ``down_weight`` is [D, H].  Optional
+    gate/down multipliers (the Falcon-H1 variant): down(SiLU(mg gate(x)) *
+    up(x)) * md, taken from the arguments or from a config's
+    ``mlp_multipliers`` pair.
     """
 
     def __init__(self, config=None, intermediate_size: int | None = None, *,
-                 hidden_size: int | None = None, dtype=torch.bfloat16, device=None):
+                 hidden_size: int | None = None, dtype=torch.bfloat16, device=None,
+                 gate_multiplier: float | None = None, down_multiplier: float | None = None):
         super().__init__()
+        mg, md = 1.0, 1.0
+        if config is not None and not isinstance(config, int):
+            mults = getattr(config, "mlp_multipliers", None)
+            if mults is not None:
+                mg, md = float(mults[0]), float(mults[1])
+        self.gate_multiplier = float(mg if gate_multiplier is None else gate_multiplier)
+        self.down_multiplier = float(md if down_multiplier is None else down_multiplier)
         # Either a transformers-style config (hidden_size, intermediate_size
         # attributes, as the xxxMLP classes take it) or the two sizes.
         if config is not None and not isinstance(config, int):
@@ -106,20 +121,25 @@ class SwiGLUMLP(torch.nn.Module):
         return self.gate_up_weight[self.intermediate_size:]
 
     @classmethod
-    def from_weights(cls, gate_weight, up_weight, down_weight):
+    def from_weights(cls, gate_weight, up_weight, down_weight, **kwargs):
         """Builds the module from three nn.Linear-style weights ([H,D], [H,D], [D,H])."""
         H, D = gate_weight.shape
-        m = cls(D, H, dtype=gate_weight.dtype, device=gate_weight.device)
+        m = cls(D, H, dtype=gate_weight.dtype, device=gate_weight.device, **kwargs)
         with torch.no_grad():
             m.gate_up_weight.copy_(torch.cat([gate_weight, up_weight], dim=0))
             m.down_weight.copy_(down_weight)
         return m
 
     def forward(self, x):
-        return swiglu_mlp(x, self.gate_up_weight, self.down_weight)
+        return swiglu_mlp(x, self.gate_up_weight, self.down_weight, self.gate_multiplier,
+                          self.down_multiplier)
 
     def extra_repr(self):
-        return "hidden_size=%d, intermediate_size=%d" % (self.hidden_size, self.intermediate_size)
+        r = "hidden_size=%d, intermediate_size=%d" % (self.hidden_size, self.intermediate_size)
+        if self.gate_multiplier != 1.0 or self.down_multiplier != 1.0:
+            r += ", gate_multiplier=%g, down_multiplier=%g" % (self.gate_multiplier,
+                                                               self.down_multiplier)
+        return r
 
 
 def _split_linear_keys(state_dict, prefix, *args, **kwargs):

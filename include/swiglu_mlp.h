@@ -198,6 +198,42 @@ swiglu_status swiglu_mlp_bwd(const void* dY, const void* X, const void* Wgu, con
                              int64_t H, swiglu_dtype dtype, void* ws, size_t ws_bytes,
                              void* stream);
 
+/* Options of the _ex entry points.  NULL options (or the base entry points)
+ * mean {1, 1, 0}: the standard MLP, gradients overwritten.
+ *
+ * gate_multiplier mg, down_multiplier md: the gate/down multiplier variant
+ * that the maintainer thread of the RFC defers to a follow-up (Falcon-H1;
+ * the pages do not define it -- this library takes the plain reading)
+ *     A = SiLU(mg * X Wg^T) * (X Wu^T),   Y = md * (A Wd^T),
+ * the stored G being the pre-activation mg * X Wg^T; backward follows the
+ * chain rule: dA = md * (dY Wd), dU = dA * SiLU(G), dG = dA * U * SiLU'(G)
+ * * mg, dWd = md * (dY^T A), dWg = dG^T X, dWu = dU^T X, dX = dG Wg + dU Wu.
+ * Both multipliers must be finite.
+ *
+ * accumulate (backward only; must be 0 for the forward calls): 1 adds the
+ * new weight gradients to the values already in dWgu and dWd (beta = 1,
+ * gradient accumulation over micro-batches), with one rounding of the fp32
+ * sum per element; dX is always overwritten. */
+typedef struct {
+  float gate_multiplier;
+  float down_multiplier;
+  int accumulate;
+} swiglu_mlp_options;
+
+swiglu_status swiglu_mlp_fwd_ex(const void* X, const void* Wgu, const void* Wd, void* Y,
+                                void* saved, int64_t M, int64_t D, int64_t H,
+                                swiglu_dtype dtype, const swiglu_mlp_options* options,
+                                void* ws, size_t ws_bytes, void* stream);
+swiglu_status swiglu_mlp_fwd_nograd_ex(const void* X, const void* Wgu, const void* Wd, void* Y,
+                                       void* A, int64_t M, int64_t D, int64_t H,
+                                       swiglu_dtype dtype, const swiglu_mlp_options* options,
+                                       void* ws, size_t ws_bytes, void* stream);
+swiglu_status swiglu_mlp_bwd_ex(const void* dY, const void* X, const void* Wgu, const void* Wd,
+                                void* saved, void* dX, void* dWgu, void* dWd, int64_t M,
+                                int64_t D, int64_t H, swiglu_dtype dtype,
+                                const swiglu_mlp_options* options, void* ws, size_t ws_bytes,
+                                void* stream);
+
 /* Synchronises ``stream`` and reads the device error word in ``ws``:
  * SWIGLU_OK, SWIGLU_ERR_DEVICE_TIMEOUT, or SWIGLU_ERR_CUDA if the stream
  * reported an error. */

@@ -106,3 +106,27 @@ def test_graph_entry_points_check_arguments_first(L):
     assert h.value is None  # nothing was created
     assert L.swiglu_mlp_graph_launch(N, N) == INVALID
     assert L.swiglu_mlp_graph_destroy(N) == INVALID
+
+
+def test_options_are_checked_before_any_launch(L):
+    good = api.Options(1.5, 0.5, 0)
+    nan = api.Options(float("nan"), 1.0, 0)
+    inf = api.Options(1.0, float("inf"), 0)
+    acc = api.Options(1.0, 1.0, 1)
+    two = api.Options(1.0, 1.0, 2)
+    fx = L.swiglu_mlp_fwd_ex
+    ngx = L.swiglu_mlp_fwd_nograd_ex
+    bx = L.swiglu_mlp_bwd_ex
+    for o in (nan, inf):
+        assert fx(P, P, P, P, P, 4, 64, 128, 0, ctypes.byref(o), P, BIG, N) == INVALID
+        assert ngx(P, P, P, P, P, 4, 64, 128, 0, ctypes.byref(o), P, BIG, N) == INVALID
+        assert bx(P, P, P, P, P, P, P, P, 4, 64, 128, 0, ctypes.byref(o), P, BIG, N) == INVALID
+    # accumulation is a backward option
+    assert fx(P, P, P, P, P, 4, 64, 128, 0, ctypes.byref(acc), P, BIG, N) == INVALID
+    assert ngx(P, P, P, P, P, 4, 64, 128, 0, ctypes.byref(acc), P, BIG, N) == INVALID
+    assert bx(P, P, P, P, P, P, P, P, 4, 64, 128, 0, ctypes.byref(two), P, BIG, N) == INVALID
+    # valid options still meet the ordinary argument checks, and M = 0 launches nothing
+    assert fx(P, P, P, P, P, 4, 60, 128, 0, ctypes.byref(good), P, BIG, N) == ALIGN
+    assert bx(N, P, P, P, P, P, P, P, 4, 64, 128, 0, ctypes.byref(acc), P, BIG, N) == INVALID
+    assert bx(P, P, P, P, P, P, P, P, 0, 64, 128, 0, ctypes.byref(acc), P, BIG, N) == OK
+    assert fx(P, P, P, P, P, 0, 64, 128, 0, N, P, BIG, N) == OK

@@ -119,5 +119,5 @@ def test_training_loop_reduces_loss():
         loss = (diff * diff).mean()
         loss.backward()
         opt.step()
-        losses.append(float(loss))
+        losses.append(float(loss.detach()))
     assert all(np.isfinite(losses)) and losses[-1] < losses[0], losses
