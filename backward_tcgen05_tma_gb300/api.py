@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
         L.swiglu_mlp_saved_bytes.argtypes = [i64, i64, ci]
         L.swiglu_mlp_workspace_bytes.restype = sz
         L.swiglu_mlp_workspace_bytes.argtypes = [i64, i64, i64, ci, ci]
+        L.swiglu_mlp_workspace_min_bytes.restype = sz
+        L.swiglu_mlp_workspace_min_bytes.argtypes = [i64, i64, i64, ci, ci]
         L.swiglu_mlp_fwd.restype = ci
         L.swiglu_mlp_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
         L.swiglu_mlp_fwd_nograd.restype = ci
@@ -153,8 +155,12 @@ def _check(code: int, where: str):
         raise SwigluError(code, where)
 
 
-def workspace(M: int, D: int, H: int, dtype: torch.dtype, op: int, device) -> torch.Tensor:
-    n = lib().swiglu_mlp_workspace_bytes(M, D, H, dtype_code(dtype), op)
+def workspace(M: int, D: int, H: int, dtype: torch.dtype, op: int, device,
+              minimal: bool = False) -> torch.Tensor:
+    """A zero-filled workspace: the recommended size, or with ``minimal`` the
+    smallest accepted one (stream-K off where its partials would not fit)."""
+    f = lib().swiglu_mlp_workspace_min_bytes if minimal else lib().swiglu_mlp_workspace_bytes
+    n = f(M, D, H, dtype_code(dtype), op)
     return torch.zeros(int(n), dtype=torch.uint8, device=device)
 
 

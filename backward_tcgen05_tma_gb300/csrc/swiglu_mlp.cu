@@ -212,6 +212,13 @@ size_t ws_clear_bytes(swiglu_dtype dt) {
   return dt == SWIGLU_F32_IEEE ? sizeof(int) : WS_HEADER + TC_SK_COUNTER_BYTES;
 }
 
+// Workspace bytes left for stream-K partial tiles after the header and the
+// tile counters.
+size_t part_capacity(size_t ws_bytes) {
+  const size_t fixed = WS_HEADER + TC_SK_COUNTER_BYTES;
+  return ws_bytes > fixed ? ws_bytes - fixed : 0;
+}
+
 size_t tc_part_bytes(const TcPlan& p) {
   return p.sk_tiles ? (size_t)p.grid * p.seg_max * TC_BM * TC_BN * 4 : 0;
 }
@@ -296,7 +303,11 @@ size_t tc_ws_part_bytes(int64_t M, int64_t D, int64_t H, int op) {
   return best;
 }
 
-TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err, bool pairs) {
+// part_cap: workspace bytes available for stream-K partial tiles; a GEMM
+// whose plan needs more runs whole tiles only (same results within
+// rounding, without the last round's balancing).
+TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err, bool pairs,
+                   size_t part_cap) {
   TcShape s;
   s.M = (int)M;
   s.N = (int)N;
@@ -314,9 +325,21 @@ TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err
                            pairs ? tc2_units() : tc_nsm());
   s.sk_tiles = p.sk_tiles;
   s.seg_max = p.seg_max;
+  if (tc_part_bytes(p) * (pairs ? 2 : 1) > part_cap) {
+    s.sk_tiles = 0;
+    s.seg_max = 1;
+  }
   s.counters = reinterpret_cast<int*>(reinterpret_cast<char*>(err) + WS_HEADER);
   s.part = reinterpret_cast<float*>(reinterpret_cast<char*>(err) + WS_HEADER + TC_SK_COUNTER_BYTES);
   return s;
+}
+
+// CTAs (or pairs) to launch: the stream-K plan's grid, or one per tile up to
+// `units` when the GEMM runs whole tiles only.
+int launch_units(const TcShape& s, int units) {
+  const int64_t tiles = (int64_t)s.m_tiles * s.n_tiles;
+  if (s.sk_tiles) return tc_plan(tiles, s.k_blocks, units).grid;
+  return (int)(tiles < units ? tiles : units);
 }
 
 // The training kernels are launched in plain stream order: with a static
@@ -330,7 +353,7 @@ cudaError_t launch_tc(int kid, const CUtensorMap& ta, const CUtensorMap& tb, con
   constexpr int smem = TcSmem<TC_BN, TC_STAGES>::DYN_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int grid = tc_plan((int64_t)s.m_tiles * s.n_tiles, s.k_blocks, tc_nsm()).grid;
+  const int grid = launch_units(s, tc_nsm());
   ProfScope prof(kid, st);
   kern<<<grid, TC_THREADS, smem, st>>>(ta, tb, s, ep);
   g_last_launches.fetch_add(1);
@@ -345,7 +368,7 @@ cudaError_t launch_tc2(int kid, const CUtensorMap& ta, const CUtensorMap& tb, co
   constexpr int smem = Tc2Smem<TC2_STAGES>::DYN_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int units = tc_plan((int64_t)s.m_tiles * s.n_tiles, s.k_blocks, tc2_units()).grid;
+  const int units = launch_units(s, tc2_units());
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * units));
   cfg.blockDim = dim3(TC_THREADS);
@@ -707,7 +730,7 @@ swiglu_status check_common(int64_t M, int64_t D, int64_t H, swiglu_dtype dt, con
   if (D % mult != 0 || H % mult != 0) return SWIGLU_ERR_ALIGNMENT;
   const int64_t lim = 0x7fffffffLL;
   if (M > lim || D > lim || 3 * H > lim) return SWIGLU_ERR_UNSUPPORTED;
-  if (ws == nullptr || ws_bytes < swiglu_mlp_workspace_bytes(M, D, H, dt, op))
+  if (ws == nullptr || ws_bytes < swiglu_mlp_workspace_min_bytes(M, D, H, dt, op))
     return SWIGLU_ERR_WORKSPACE;
   if (!aligned16(ws)) return SWIGLU_ERR_ALIGNMENT;
   return SWIGLU_OK;
@@ -746,7 +769,8 @@ swiglu_status read_opts(const swiglu_mlp_options* in, bool backward, Opts* out) 
 template <bool BF16>
 swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y, void* G,
                          void* U, int64_t ld_gu, void* A, int64_t ld_a, int64_t M, int64_t D,
-                         int64_t H, int* err, const Opts& o, cudaStream_t st) {
+                         int64_t H, int* err, size_t ws_bytes, const Opts& o, cudaStream_t st) {
+  const size_t cap = part_capacity(ws_bytes);
   CUtensorMap tx, tw, ta, twd;
   // gate/up + SwiGLU: C[m, j | H + j], N counts hidden units, BN/2 per tile;
   // on a pair each CTA brings one of Wg, Wu
@@ -754,7 +778,7 @@ swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y
   if (!map_kmajor(&tx, BF16, X, D, M, D, TC_BM) ||
       !encode_gateup(&tw, BF16, Wgu, D, H, TC_BN / 2, pairs1 ? 1 : 2))
     return SWIGLU_ERR_CUDA;
-  TcShape s1 = make_shape(M, H, D, TC_BN / 2, err, pairs1);
+  TcShape s1 = make_shape(M, H, D, TC_BN / 2, err, pairs1, cap);
   EpiSwiGLU::Params p1{G, U, ld_gu, A, ld_a, o.gm};
   cudaError_t e = launch_gemm<LOAD_KMAJOR, LOAD_GATEUP, BF16, EpiSwiGLU>(
       pairs1, G != nullptr ? K_GATE_UP : K_GATE_UP_NOGRAD, tx, tw, s1, p1, st);
@@ -765,7 +789,7 @@ swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y
   if (!map_kmajor(&ta, BF16, A, H, M, ld_a, TC_BM) ||
       !map_kmajor(&twd, BF16, Wd, H, D, H, pairs2 ? 128 : TC_BN))
     return SWIGLU_ERR_CUDA;
-  TcShape s2 = make_shape(M, D, H, TC_BN, err, pairs2);
+  TcShape s2 = make_shape(M, D, H, TC_BN, err, pairs2, cap);
   EpiStore::Params p2{Y, D, o.dm, 0};
   return cuda_status(launch_gemm<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore>(
       pairs2, G != nullptr ? K_DOWN : K_DOWN_NOGRAD, ta, twd, s2, p2, st));
@@ -774,7 +798,9 @@ swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y
 template <bool BF16>
 swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const void* Wd,
                           void* saved, void* dX, void* dWgu, void* dWd, int64_t M, int64_t D,
-                          int64_t H, int* err, const Opts& o, cudaStream_t st) {
+                          int64_t H, int* err, size_t ws_bytes, const Opts& o,
+                          cudaStream_t st) {
+  const size_t cap = part_capacity(ws_bytes);
   const int64_t ld = 3 * H;
   char* sv = static_cast<char*>(saved);
   void* G = sv;
@@ -787,7 +813,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     return SWIGLU_ERR_CUDA;
   {
     const bool pairs = use_pairs(D, H, TC_BN, M);
-    TcShape s = make_shape(D, H, M, TC_BN, err, pairs);
+    TcShape s = make_shape(D, H, M, TC_BN, err, pairs, cap);
     EpiStore::Params p{dWd, H, o.dm, o.acc};
     e = launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWD, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
@@ -797,7 +823,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     return SWIGLU_ERR_CUDA;
   {
     const bool pairs = use_pairs(M, H, TC_BN, D);
-    TcShape s = make_shape(M, H, D, TC_BN, err, pairs);
+    TcShape s = make_shape(M, H, D, TC_BN, err, pairs, cap);
     EpiDSwiGLU::Params p{G, U, ld, o.gm, o.dm};
     e = launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLU>(pairs, K_DGU, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
@@ -807,7 +833,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     return SWIGLU_ERR_CUDA;
   {
     const bool pairs = use_pairs(2 * H, D, TC_BN, M);
-    TcShape s = make_shape(2 * H, D, M, TC_BN, err, pairs);
+    TcShape s = make_shape(2 * H, D, M, TC_BN, err, pairs, cap);
     EpiStore::Params p{dWgu, D, 1.0f, o.acc};
     e = launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWGU, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
@@ -817,7 +843,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     return SWIGLU_ERR_CUDA;
   {
     const bool pairs = use_pairs(M, D, TC_BN, 2 * H);
-    TcShape s = make_shape(M, D, 2 * H, TC_BN, err, pairs);
+    TcShape s = make_shape(M, D, 2 * H, TC_BN, err, pairs, cap);
     EpiStore::Params p{dX, D, 1.0f, 0};
     e = launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DX, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
@@ -890,6 +916,14 @@ size_t swiglu_mlp_workspace_bytes(int64_t M, int64_t D, int64_t H, swiglu_dtype 
   return WS_HEADER;
 }
 
+size_t swiglu_mlp_workspace_min_bytes(int64_t M, int64_t D, int64_t H, swiglu_dtype dtype,
+                                      int op) {
+  if (op == SWIGLU_OP_FWD_NOGRAD && D > 0 && H > 0 && ng_eligible(M, D, H, dtype))
+    return ng_two_bytes(ng_plan(M, D, H));
+  if (dtype == SWIGLU_BF16 || dtype == SWIGLU_F16) return WS_HEADER + TC_SK_COUNTER_BYTES;
+  return WS_HEADER;
+}
+
 swiglu_status swiglu_mlp_fwd_ex(const void* X, const void* Wgu, const void* Wd, void* Y,
                                 void* saved, int64_t M, int64_t D, int64_t H,
                                 swiglu_dtype dtype, const swiglu_mlp_options* options,
@@ -912,9 +946,9 @@ swiglu_status swiglu_mlp_fwd_ex(const void* X, const void* Wgu, const void* Wd, 
   void* A = sv + 2 * H * e;
   switch (dtype) {
     case SWIGLU_BF16:
-      return tc_forward<true>(X, Wgu, Wd, Y, G, U, 3 * H, A, 3 * H, M, D, H, err, o, s);
+      return tc_forward<true>(X, Wgu, Wd, Y, G, U, 3 * H, A, 3 * H, M, D, H, err, ws_bytes, o, s);
     case SWIGLU_F16:
-      return tc_forward<false>(X, Wgu, Wd, Y, G, U, 3 * H, A, 3 * H, M, D, H, err, o, s);
+      return tc_forward<false>(X, Wgu, Wd, Y, G, U, 3 * H, A, 3 * H, M, D, H, err, ws_bytes, o, s);
     default:
       return simt_forward((const float*)X, (const float*)Wgu, (const float*)Wd, (float*)Y,
                           (float*)G, (float*)U, 3 * H, (float*)A, 3 * H, M, D, H, o, s);
@@ -950,9 +984,9 @@ swiglu_status swiglu_mlp_fwd_nograd_ex(const void* X, const void* Wgu, const voi
   if (cudaMemsetAsync(err, 0, ws_clear_bytes(dtype), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
   switch (dtype) {
     case SWIGLU_BF16:
-      return tc_forward<true>(X, Wgu, Wd, Y, nullptr, nullptr, 0, A, H, M, D, H, err, o, s);
+      return tc_forward<true>(X, Wgu, Wd, Y, nullptr, nullptr, 0, A, H, M, D, H, err, ws_bytes, o, s);
     case SWIGLU_F16:
-      return tc_forward<false>(X, Wgu, Wd, Y, nullptr, nullptr, 0, A, H, M, D, H, err, o, s);
+      return tc_forward<false>(X, Wgu, Wd, Y, nullptr, nullptr, 0, A, H, M, D, H, err, ws_bytes, o, s);
     default:
       return simt_forward((const float*)X, (const float*)Wgu, (const float*)Wd, (float*)Y,
                           nullptr, nullptr, 0, (float*)A, H, M, D, H, o, s);
@@ -1011,9 +1045,9 @@ swiglu_status swiglu_mlp_bwd_ex(const void* dY, const void* X, const void* Wgu, 
   if (cudaMemsetAsync(err, 0, ws_clear_bytes(dtype), s) != cudaSuccess) return SWIGLU_ERR_CUDA;
   switch (dtype) {
     case SWIGLU_BF16:
-      return tc_backward<true>(dY, X, Wgu, Wd, saved, dX, dWgu, dWd, M, D, H, err, o, s);
+      return tc_backward<true>(dY, X, Wgu, Wd, saved, dX, dWgu, dWd, M, D, H, err, ws_bytes, o, s);
     case SWIGLU_F16:
-      return tc_backward<false>(dY, X, Wgu, Wd, saved, dX, dWgu, dWd, M, D, H, err, o, s);
+      return tc_backward<false>(dY, X, Wgu, Wd, saved, dX, dWgu, dWd, M, D, H, err, ws_bytes, o, s);
     default:
       return simt_backward((const float*)dY, (const float*)X, (const float*)Wgu,
                            (const float*)Wd, (float*)saved, (float*)dX, (float*)dWgu,

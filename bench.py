@@ -204,15 +204,17 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def _alloc(M, D, H, dt, device):
+def _alloc(M, D, H, dt, device, minimal_ws=False):
     import torch
     from backward_tcgen05_tma_gb300 import api
+    size = api.lib().swiglu_mlp_workspace_min_bytes if minimal_ws else \
+        api.lib().swiglu_mlp_workspace_bytes
     e = {"Y": torch.empty(M, D, dtype=dt, device=device),
          "saved": torch.empty(M, 3 * H, dtype=dt, device=device),
          "dX": torch.empty(M, D, dtype=dt, device=device),
          "dWgu": torch.empty(2 * H, D, dtype=dt, device=device),
          "dWd": torch.empty(D, H, dtype=dt, device=device)}
-    e["ws"] = torch.zeros(max(api.lib().swiglu_mlp_workspace_bytes(M, D, H, api.dtype_code(dt), op)
+    e["ws"] = torch.zeros(max(size(M, D, H, api.dtype_code(dt), op)
                               for op in (api.SWIGLU_OP_FWD, api.SWIGLU_OP_BWD)),
                           dtype=torch.uint8, device=device)
     return e
@@ -231,7 +233,8 @@ def _kernel_flops(name, M, D, H):
             "dwgu": 2.0 * 2 * H * D * M, "dx": 2.0 * M * D * 2 * H}[name]
 
 
-def _time_training(api, w, dtype_name, steps, warmup, seed, device, profile=False):
+def _time_training(api, w, dtype_name, steps, warmup, seed, device, profile=False,
+                   minimal_ws=False):
     """Times `steps` fwd+bwd steps (CUDA events on the launching stream);
     returns (seconds per step, kernel launches, per-kernel profile, buffers).
 
@@ -244,7 +247,7 @@ def _time_training(api, w, dtype_name, steps, warmup, seed, device, profile=Fals
     dt = {"bf16": torch.bfloat16, "f16": torch.float16}[dtype_name]
     M, D, H = w["B"] * w["S"], w["D"], w["H"]
     t = synthetic.make_inputs(M, D, H, dtype_name, seed=seed, device=device, kind="device")
-    o = _alloc(M, D, H, dt, device)
+    o = _alloc(M, D, H, dt, device, minimal_ws)
     for _ in range(warmup):
         _step(api, t, o)
     torch.cuda.synchronize()
@@ -413,6 +416,37 @@ def _decode_loop(api, X, wts, o, ws):
     return out
 
 
+# The pages' training intermediate memory (MB as printed), fwd+bwd, bf16, B=8,
+# D=4096, H=11008: fused implementation and Liger, by sequence length.
+PAGES_TRAIN_MEMORY = {256: (178.0, 107.0), 8192: (5664.0, 6356.0)}
+
+
+def _memory_report(api, w, device):
+    """Training intermediates (the [G|U|A] buffer + workspace) at the pages'
+    memory-table shapes, with the recommended and the minimal workspace, and
+    the main workload's step time with the minimal workspace."""
+    import torch
+    L = api.lib()
+    D, H = w["D"], w["H"]
+    rows = {}
+    for S, (flash, liger) in PAGES_TRAIN_MEMORY.items():
+        M = 8 * S
+        saved = L.swiglu_mlp_saved_bytes(M, H, 0)
+        full = max(L.swiglu_mlp_workspace_bytes(M, D, H, 0, op) for op in (0, 2))
+        least = max(L.swiglu_mlp_workspace_min_bytes(M, D, H, 0, op) for op in (0, 2))
+        mib = 1.0 / 2 ** 20
+        rows["B8_S%d_D%d_H%d" % (S, D, H)] = {
+            "saved_MiB": round(saved * mib, 1), "ws_MiB": round(full * mib, 1),
+            "ws_min_MiB": round(least * mib, 3), "total_MiB": round((saved + full) * mib, 1),
+            "total_min_ws_MiB": round((saved + least) * mib, 1),
+            "pages_MB": {"fused": flash, "liger": liger}}
+    sec, _, _, keep = _time_training(api, w, "bf16", 10, 3, 0, device, minimal_ws=True)
+    del keep
+    torch.cuda.empty_cache()
+    return {"intermediates": rows, "unit_note": "MiB = 2^20 bytes; the pages print MB",
+            "main_workload_min_ws_ms_per_step": round(sec * 1e3, 3)}
+
+
 def _cpu_baseline(t_dev, w):
     """The oracle, as it stands, on a bounded sample: fwd+bwd of the first
     CPU_SAMPLE_TOKENS token rows of the workload with its full weights."""
@@ -534,6 +568,7 @@ def run_ours(args):
                     "kernel_ms": {k: round(v[1] / v[0], 4) for k, v in prof2.items()}}
                 torch.cuda.empty_cache()
         line["other_workloads"] = extra
+        line["memory"] = _memory_report(api, w, device)
         line["nograd"] = _nograd_sweep(api, device, peaks)
     if world == 1 or rank == 0:
         if world == 1 and not args.no_cpu:

@@ -39,8 +39,9 @@
  * fp32 D and H must be multiples of 4.  M = 0 returns SWIGLU_OK and launches
  * nothing.  ``stream`` is a cudaStream_t (0 = legacy default stream).
  *
- * Workspace: ``ws`` is a device buffer of at least swiglu_mlp_workspace_bytes()
- * bytes (a size for the current device), owned by the caller, ZERO-FILLED
+ * Workspace: ``ws`` is a device buffer of swiglu_mlp_workspace_bytes() bytes
+ * (a size for the current device; at least swiglu_mlp_workspace_min_bytes()
+ * is accepted, see there), owned by the caller, ZERO-FILLED
  * before its first use.  It holds a device error word (cleared at the start
  * of every call), per-tile arrival counters (cleared by every training call,
  * left at zero by every completed few-token no-grad call) and fp32 partial
@@ -96,8 +97,21 @@ size_t swiglu_mlp_element_bytes(swiglu_dtype dtype);
 size_t swiglu_mlp_saved_bytes(int64_t M, int64_t H, swiglu_dtype dtype);
 
 /* Bytes of workspace an operation needs (at least the 256-byte header that
- * holds the device error word). */
+ * holds the device error word), with room for every GEMM's stream-K partial
+ * tiles and, for few tokens without gradients, for either kernel form. */
 size_t swiglu_mlp_workspace_bytes(int64_t M, int64_t D, int64_t H, swiglu_dtype dtype, int op);
+
+/* The smallest workspace an operation accepts: the header and tile counters
+ * (1.25 KB) for the tensor-core paths, plus the two-kernel form's partial
+ * tiles for few tokens without gradients.  With less than
+ * swiglu_mlp_workspace_bytes(), each GEMM whose stream-K partial tiles do
+ * not fit runs whole tiles only (results within the same tolerances; the
+ * last round of tiles is no longer balanced over the SMs), and the few-token
+ * no-grad call takes the fused kernel only if its partials fit.  This trades
+ * a few percent of speed for up to ~40 MB at the largest shapes (training
+ * intermediates at small S are then the [G|U|A] buffer alone). */
+size_t swiglu_mlp_workspace_min_bytes(int64_t M, int64_t D, int64_t H, swiglu_dtype dtype,
+                                      int op);
 
 /* Training forward.  Writes Y [M,D] and saved [M,3H] = [G | U | A].
  * Reads X [M,D], Wgu [2H,D], Wd [D,H].  ("Summary": the gate and up

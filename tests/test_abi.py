@@ -75,11 +75,15 @@ def test_argument_errors_are_reported_before_any_launch(L):
     assert L.swiglu_mlp_fwd_nograd(P, P, P, P, P, 4, 64, 128, 0, P, 256, N) == WSERR
     assert L.swiglu_mlp_bwd(P, P, P, P, P, P, P, N, 4, 64, 128, 0, P, BIG, N) == INVALID
     assert L.swiglu_mlp_bwd(P, P, P, P, P, P, P, P_MIS, 4, 64, 128, 0, P, BIG, N) == ALIGN
-    # the workspace must hold the error word, the shared-tile counters and the
-    # stream-K partial tiles
+    # the workspace must hold at least the error word and the shared-tile
+    # counters; the recommended size adds the stream-K partial tiles
     need = L.swiglu_mlp_workspace_bytes(128, 64, 128, 0, 0)
-    assert need > 256
-    assert _fwd(L, wsb=need - 1) == WSERR
+    least = L.swiglu_mlp_workspace_min_bytes(128, 64, 128, 0, 0)
+    assert need >= least > 256
+    assert _fwd(L, wsb=least - 1) == WSERR
+    assert L.swiglu_mlp_fwd_nograd(P, P, P, P, P, 4, 64, 128, 0, P,
+                                   L.swiglu_mlp_workspace_min_bytes(4, 64, 128, 0, 1) - 1,
+                                   N) == WSERR
 
 
 def test_empty_batch_is_ok_without_launch(L):

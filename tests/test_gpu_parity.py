@@ -409,3 +409,40 @@ def test_stream_k_shared_tiles_parity_and_determinism(cta_pairs):
     for k in a:
         np.testing.assert_array_equal(a[k], b[k])
     check_all(a, run_oracle(t, "bf16"), "bf16")
+
+
+def test_minimal_workspace_parity(cta_pairs):
+    """With the smallest accepted workspace the GEMMs run whole tiles only
+    (no stream-K partials): same results within the tolerances, and the
+    few-token no-grad call falls back to the two-kernel form."""
+    M, D, H = 1024, 512, 1024
+    t = synthetic.make_inputs(M, D, H, "bf16", seed=70, device="cuda")
+    full = run_gpu(t, "bf16")
+    L = api.lib()
+    ws_f = api.workspace(M, D, H, torch.bfloat16, api.SWIGLU_OP_FWD, "cuda", minimal=True)
+    ws_b = api.workspace(M, D, H, torch.bfloat16, api.SWIGLU_OP_BWD, "cuda", minimal=True)
+    assert ws_f.numel() < L.swiglu_mlp_workspace_bytes(M, D, H, 0, api.SWIGLU_OP_BWD)
+    Y, saved = api.swiglu_mlp_fwd(t["X"], t["Wgu"], t["Wd"], ws=ws_f)
+    fs = saved.clone()
+    dX, dWgu, dWd = api.swiglu_mlp_bwd(t["dY"], t["X"], t["Wgu"], t["Wd"], saved, ws=ws_b)
+    torch.cuda.synchronize()
+    assert api.swiglu_mlp_query_error(ws_b) == 0
+    small = {"Y": f64(Y), "G": f64(fs[:, :H]), "U": f64(fs[:, H:2 * H]), "A": f64(fs[:, 2 * H:]),
+             "dG": f64(saved[:, :H]), "dU": f64(saved[:, H:2 * H]), "dX": f64(dX),
+             "dWg": f64(dWgu[:H]), "dWu": f64(dWgu[H:]), "dWd": f64(dWd)}
+    check_all(small, run_oracle(t, "bf16"), "bf16")
+    for k in small:
+        assert oracle.rel_frob(small[k], full[k]) <= 1e-2, k
+    # few tokens: the minimal workspace fits the two-kernel form
+    tn = synthetic.make_inputs(16, 4096, 11008, "bf16", seed=71, device="cuda", kind="device")
+    ws_n = api.workspace(16, 4096, 11008, torch.bfloat16, api.SWIGLU_OP_FWD_NOGRAD, "cuda",
+                         minimal=True)
+    old = api.swiglu_mlp_set_nograd_fused(2)
+    try:
+        Yn, _ = api.swiglu_mlp_fwd_nograd(tn["X"], tn["Wgu"], tn["Wd"], ws=ws_n)
+        assert api.swiglu_mlp_last_launch_count() in (1, 2)
+        Yr, _ = api.swiglu_mlp_fwd_nograd(tn["X"], tn["Wgu"], tn["Wd"])
+    finally:
+        api.swiglu_mlp_set_nograd_fused(old)
+    torch.cuda.synchronize()
+    assert oracle.rel_frob(f64(Yn), f64(Yr)) <= 1e-2
