@@ -825,7 +825,11 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     const bool pairs = use_pairs(M, H, TC_BN, D);
     TcShape s = make_shape(M, H, D, TC_BN, err, pairs, cap);
     EpiDSwiGLU::Params p{G, U, ld, o.gm, o.dm};
-    e = launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLU>(pairs, K_DGU, m1, m2, s, p, st);
+    // a short contraction leaves the epilogue the bound: direct G/U loads
+    e = D <= 2048 ? launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLUT<true>>(
+                        pairs, K_DGU, m1, m2, s, p, st)
+                  : launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLUT<false>>(
+                        pairs, K_DGU, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   // [dWg; dWu] [2H, D] = [dG | dU]^T X: one GEMM over the 2H columns
