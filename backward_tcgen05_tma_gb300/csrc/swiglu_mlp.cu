@@ -272,9 +272,13 @@ bool use_pairs(int64_t Mg, int64_t N, int64_t n_per_tile, int64_t K) {
   const int mode = g_cta_pairs.load();
   if (mode == 0 || tc2_units() < 1) return false;
   if (mode == 2) return true;
-  const int64_t tiles = ((Mg + TC_BM - 1) / TC_BM) * ((N + n_per_tile - 1) / n_per_tile);
+  // pairs once every pair gets at least one of their 256-row tiles; measured
+  // per GEMM at B=8, S=2048-8192 (D = 1024-4096): as fast or faster on
+  // pairs for every GEMM there, including the short contractions (gate/up
+  // and dX at D = 1024: 0.151 vs 0.171 and 0.126 vs 0.143 ms)
+  const int64_t pair_tiles = ((Mg + TC2_BM - 1) / TC2_BM) * ((N + n_per_tile - 1) / n_per_tile);
   const int64_t kb = (K + TC_BK - 1) / TC_BK;
-  return (kb >= 32 && tiles >= 4 * (int64_t)tc_nsm()) || kb >= 256;
+  return (kb >= 16 && pair_tiles >= (int64_t)tc2_units()) || kb >= 256;
 }
 
 // pairs: tiles of 256 rows handed out per CTA pair (tc2_gemm_kernel).
