@@ -272,13 +272,17 @@ bool use_pairs(int64_t Mg, int64_t N, int64_t n_per_tile, int64_t K) {
   const int mode = g_cta_pairs.load();
   if (mode == 0 || tc2_units() < 1) return false;
   if (mode == 2) return true;
-  // pairs once every pair gets at least one of their 256-row tiles; measured
-  // per GEMM at B=8, S=2048-8192 (D = 1024-4096): as fast or faster on
-  // pairs for every GEMM there, including the short contractions (gate/up
-  // and dX at D = 1024: 0.151 vs 0.171 and 0.126 vs 0.143 ms)
+  // pairs once every pair gets at least one of their 256-row tiles and the
+  // 256-row tiles add no padding beyond the 128-row ones; measured per GEMM
+  // at B=8, S=2048-8192 (D = 1024-4096): as fast or faster on pairs for
+  // every GEMM there, including the short contractions (gate/up and dX at
+  // D = 1024: 0.151 vs 0.171 and 0.126 vs 0.143 ms); no-grad calls with
+  // 65-128 or 384 tokens, whose pair tiles would be partly empty, are 3% and
+  // 11% faster on single SMs
   const int64_t pair_tiles = ((Mg + TC2_BM - 1) / TC2_BM) * ((N + n_per_tile - 1) / n_per_tile);
+  const bool no_pad = (Mg + TC2_BM - 1) / TC2_BM * TC2_BM == (Mg + TC_BM - 1) / TC_BM * TC_BM;
   const int64_t kb = (K + TC_BK - 1) / TC_BK;
-  return (kb >= 16 && pair_tiles >= (int64_t)tc2_units()) || kb >= 256;
+  return (kb >= 16 && no_pad && pair_tiles >= (int64_t)tc2_units()) || kb >= 256;
 }
 
 // pairs: tiles of 256 rows handed out per CTA pair (tc2_gemm_kernel).

@@ -273,8 +273,9 @@ void swiglu_mlp_inject_stall_once(int on);
  * GEMMs: on pairs of SMs -- 2-CTA clusters issuing tcgen05.mma.cta_group::2
  * on 256 x 256 tiles, each SM loading half of each operand tile -- or on
  * single SMs (128 x 256 tiles).  mode 1 (the default): pairs for the GEMMs
- * with enough 256 x 256 tiles to give every pair one (and K >= 1024), or
- * with K >= 16384; 2: pairs for every GEMM; 0: never.  All modes give
+ * with enough 256 x 256 tiles to give every pair one, K >= 1024 and rows
+ * that 256-row tiles cover without more padding than 128-row ones, or with
+ * K >= 16384; 2: pairs for every GEMM; 0: never.  All modes give
  * results within the same tolerances (accumulation order differs).  Returns
  * the previous mode.  A workspace sized by swiglu_mlp_workspace_bytes() fits
  * every mode. */
