@@ -24,18 +24,22 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libswiglu_mlp.so")
+# the same library compiled with -DSWIGLU_DEBUG (device index checks)
+DEBUG_LIB_PATH = os.path.join(_HERE, "libswiglu_mlp_debug.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "swiglu_mlp.h")
 
 SWIGLU_BF16, SWIGLU_F16, SWIGLU_F32_IEEE = 0, 1, 2
 SWIGLU_OP_FWD, SWIGLU_OP_FWD_NOGRAD, SWIGLU_OP_BWD = 0, 1, 2
 STATUS = {0: "SWIGLU_OK", 1: "SWIGLU_ERR_INVALID_ARG", 2: "SWIGLU_ERR_ALIGNMENT",
           3: "SWIGLU_ERR_UNSUPPORTED", 4: "SWIGLU_ERR_WORKSPACE", 5: "SWIGLU_ERR_CUDA",
-          6: "SWIGLU_ERR_DEVICE_TIMEOUT"}
+          6: "SWIGLU_ERR_DEVICE_TIMEOUT", 7: "SWIGLU_ERR_DEVICE_BOUNDS"}
 
 _DT = {torch.bfloat16: SWIGLU_BF16, torch.float16: SWIGLU_F16, torch.float32: SWIGLU_F32_IEEE}
 
 _lock = threading.Lock()
 _lib = None
+_loaded = {}  # path -> CDLL
+_use_debug = False
 
 
 class SwigluError(RuntimeError):
@@ -58,70 +62,97 @@ def _opts(gate_mul: float, down_mul: float, accumulate: bool):
 
 
 def lib() -> ctypes.CDLL:
-    """The loaded CUDA library (raises if it has not been built)."""
+    """The loaded CUDA library (raises if it has not been built): the release
+    build, or the debug build while use_debug_library(True) is in effect."""
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        if not os.path.exists(LIB_PATH):
-            raise ImportError("libswiglu_mlp.so is not built (run __graft_entry__.build() or "
-                              "python -m backward_tcgen05_tma_gb300.build); no fallback exists")
-        L = ctypes.CDLL(LIB_PATH)
-        vp, i64, ci, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
-        L.swiglu_mlp_element_bytes.restype = sz
-        L.swiglu_mlp_element_bytes.argtypes = [ci]
-        L.swiglu_mlp_saved_bytes.restype = sz
-        L.swiglu_mlp_saved_bytes.argtypes = [i64, i64, ci]
-        L.swiglu_mlp_workspace_bytes.restype = sz
-        L.swiglu_mlp_workspace_bytes.argtypes = [i64, i64, i64, ci, ci]
-        L.swiglu_mlp_workspace_min_bytes.restype = sz
-        L.swiglu_mlp_workspace_min_bytes.argtypes = [i64, i64, i64, ci, ci]
-        L.swiglu_mlp_fwd.restype = ci
-        L.swiglu_mlp_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
-        L.swiglu_mlp_fwd_nograd.restype = ci
-        L.swiglu_mlp_fwd_nograd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
-        L.swiglu_mlp_fwd_nograd_noalloc.restype = ci
-        L.swiglu_mlp_fwd_nograd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
-        L.swiglu_mlp_graph_create_fwd_nograd.restype = ci
-        L.swiglu_mlp_graph_create_fwd_nograd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp,
-                                                         sz, ctypes.POINTER(vp)]
-        L.swiglu_mlp_graph_launch.restype = ci
-        L.swiglu_mlp_graph_launch.argtypes = [vp, vp]
-        L.swiglu_mlp_graph_destroy.restype = ci
-        L.swiglu_mlp_graph_destroy.argtypes = [vp]
-        op = ctypes.c_void_p
-        L.swiglu_mlp_fwd_ex.restype = ci
-        L.swiglu_mlp_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, op, vp, sz, vp]
-        L.swiglu_mlp_fwd_nograd_ex.restype = ci
-        L.swiglu_mlp_fwd_nograd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, op, vp, sz,
-                                               vp]
-        L.swiglu_mlp_bwd_ex.restype = ci
-        L.swiglu_mlp_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, op, vp,
-                                        sz, vp]
-        L.swiglu_mlp_bwd.restype = ci
-        L.swiglu_mlp_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
-        L.swiglu_mlp_query_error.restype = ci
-        L.swiglu_mlp_query_error.argtypes = [vp, vp]
-        L.swiglu_status_string.restype = ctypes.c_char_p
-        L.swiglu_status_string.argtypes = [ci]
-        L.swiglu_mlp_set_wait_limit_ns.restype = ctypes.c_uint64
-        L.swiglu_mlp_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
-        L.swiglu_mlp_inject_stall_once.restype = None
-        L.swiglu_mlp_inject_stall_once.argtypes = [ci]
-        L.swiglu_mlp_last_launch_count.restype = ci
-        L.swiglu_mlp_last_launch_count.argtypes = []
-        L.swiglu_mlp_set_cta_pairs.restype = ci
-        L.swiglu_mlp_set_cta_pairs.argtypes = [ci]
-        L.swiglu_mlp_set_nograd_fused.restype = ci
-        L.swiglu_mlp_set_nograd_fused.argtypes = [ci]
-        L.swiglu_mlp_profile_enable.restype = None
-        L.swiglu_mlp_profile_enable.argtypes = [ci]
-        L.swiglu_mlp_profile_read.restype = ci
-        L.swiglu_mlp_profile_read.argtypes = [ci, vp, vp]
-        L.swiglu_mlp_kernel_name.restype = ctypes.c_char_p
-        L.swiglu_mlp_kernel_name.argtypes = [ci]
-        _lib = L
-        return L
+        if _lib is None:
+            _lib = _load(DEBUG_LIB_PATH if _use_debug else LIB_PATH)
+        return _lib
+
+
+def use_debug_library(on: bool) -> bool:
+    """Routes every later call of this module to the debug build
+    (libswiglu_mlp_debug.so: device index checks, SWIGLU_ERR_DEVICE_BOUNDS)
+    or back to the release build; returns the previous setting.  Both stay
+    loaded; each keeps its own process-wide settings (wait limit, SM-pair
+    and few-token modes)."""
+    global _lib, _use_debug
+    with _lock:
+        prev = _use_debug
+        _use_debug = bool(on)
+        _lib = None
+    lib()
+    return prev
+
+
+def _load(path: str) -> ctypes.CDLL:
+    if path in _loaded:
+        return _loaded[path]
+    if not os.path.exists(path):
+        raise ImportError("%s is not built (run __graft_entry__.build() or python -m "
+                          "backward_tcgen05_tma_gb300.build); no fallback exists"
+                          % os.path.basename(path))
+    L = ctypes.CDLL(path)
+    vp, i64, ci, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    L.swiglu_mlp_element_bytes.restype = sz
+    L.swiglu_mlp_element_bytes.argtypes = [ci]
+    L.swiglu_mlp_saved_bytes.restype = sz
+    L.swiglu_mlp_saved_bytes.argtypes = [i64, i64, ci]
+    L.swiglu_mlp_workspace_bytes.restype = sz
+    L.swiglu_mlp_workspace_bytes.argtypes = [i64, i64, i64, ci, ci]
+    L.swiglu_mlp_workspace_min_bytes.restype = sz
+    L.swiglu_mlp_workspace_min_bytes.argtypes = [i64, i64, i64, ci, ci]
+    L.swiglu_mlp_fwd.restype = ci
+    L.swiglu_mlp_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
+    L.swiglu_mlp_fwd_nograd.restype = ci
+    L.swiglu_mlp_fwd_nograd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
+    L.swiglu_mlp_fwd_nograd_noalloc.restype = ci
+    L.swiglu_mlp_fwd_nograd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
+    L.swiglu_mlp_graph_create_fwd_nograd.restype = ci
+    L.swiglu_mlp_graph_create_fwd_nograd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp,
+                                                     sz, ctypes.POINTER(vp)]
+    L.swiglu_mlp_graph_launch.restype = ci
+    L.swiglu_mlp_graph_launch.argtypes = [vp, vp]
+    L.swiglu_mlp_graph_destroy.restype = ci
+    L.swiglu_mlp_graph_destroy.argtypes = [vp]
+    op = ctypes.c_void_p
+    L.swiglu_mlp_fwd_ex.restype = ci
+    L.swiglu_mlp_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, op, vp, sz, vp]
+    L.swiglu_mlp_fwd_nograd_ex.restype = ci
+    L.swiglu_mlp_fwd_nograd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, op, vp, sz,
+                                           vp]
+    L.swiglu_mlp_bwd_ex.restype = ci
+    L.swiglu_mlp_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, op, vp,
+                                    sz, vp]
+    L.swiglu_mlp_bwd.restype = ci
+    L.swiglu_mlp_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
+    L.swiglu_mlp_query_error.restype = ci
+    L.swiglu_mlp_query_error.argtypes = [vp, vp]
+    L.swiglu_status_string.restype = ctypes.c_char_p
+    L.swiglu_status_string.argtypes = [ci]
+    L.swiglu_mlp_set_wait_limit_ns.restype = ctypes.c_uint64
+    L.swiglu_mlp_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.swiglu_mlp_inject_stall_once.restype = None
+    L.swiglu_mlp_inject_stall_once.argtypes = [ci]
+    L.swiglu_mlp_last_launch_count.restype = ci
+    L.swiglu_mlp_last_launch_count.argtypes = []
+    L.swiglu_mlp_set_cta_pairs.restype = ci
+    L.swiglu_mlp_set_cta_pairs.argtypes = [ci]
+    L.swiglu_mlp_set_nograd_fused.restype = ci
+    L.swiglu_mlp_set_nograd_fused.argtypes = [ci]
+    L.swiglu_mlp_profile_enable.restype = None
+    L.swiglu_mlp_profile_enable.argtypes = [ci]
+    L.swiglu_mlp_profile_read.restype = ci
+    L.swiglu_mlp_profile_read.argtypes = [ci, vp, vp]
+    L.swiglu_mlp_kernel_name.restype = ctypes.c_char_p
+    L.swiglu_mlp_kernel_name.argtypes = [ci]
+    L.swiglu_mlp_debug_build.restype = ci
+    L.swiglu_mlp_debug_build.argtypes = []
+    L.swiglu_mlp_debug_narrow_once.restype = None
+    L.swiglu_mlp_debug_narrow_once.argtypes = [ci]
+    _loaded[path] = L
+    return L
 
 
 def declared_symbols() -> list[str]:

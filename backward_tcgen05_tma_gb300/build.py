@@ -1,6 +1,9 @@
-"""Builds libswiglu_mlp.so in place with nvcc for sm_103a (GB300)."""
+"""Builds libswiglu_mlp.so (release) and libswiglu_mlp_debug.so (the same
+sources with -DSWIGLU_DEBUG: device index checks) in place with nvcc for
+sm_103a (GB300).  The two compile in parallel."""
 from __future__ import annotations
 
+import glob
 import os
 import subprocess
 
@@ -8,8 +11,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 SO = os.path.join(HERE, "libswiglu_mlp.so")
+SO_DEBUG = os.path.join(HERE, "libswiglu_mlp_debug.so")
 SOURCES = ["swiglu_mlp.cu"]
-HEADERS = ["sm103_ptx.cuh", "tc_gemm.cuh", "tc2_gemm.cuh", "simt_gemm.cuh", "ng_gemm.cuh"]
 
 NVCC_FLAGS = [
     "-std=c++17", "-O3", "-lineinfo",
@@ -23,26 +26,37 @@ def _nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def _stale() -> bool:
-    if not os.path.exists(SO):
+def _stale(so: str) -> bool:
+    if not os.path.exists(so):
         return True
-    t = os.path.getmtime(SO)
-    deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
+    t = os.path.getmtime(so)
+    deps = [os.path.join(CSRC, f) for f in SOURCES]
+    deps += glob.glob(os.path.join(CSRC, "*.cuh"))
     deps.append(os.path.join(ROOT, "include", "swiglu_mlp.h"))
     deps.append(os.path.abspath(__file__))
     return any(os.path.getmtime(d) > t for d in deps)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the CUDA library if missing or out of date; returns its path."""
-    if not force and not _stale():
-        return SO
-    tmp = SO + ".%d.tmp" % os.getpid()
-    cmd = [_nvcc(), *NVCC_FLAGS, "-o", tmp] + [os.path.join(CSRC, f) for f in SOURCES]
-    if verbose:
-        print(" ".join(cmd))
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, SO)
+    """Compile whichever of the two libraries is missing or out of date;
+    returns the release library's path."""
+    jobs = []
+    for so, extra in ((SO, []), (SO_DEBUG, ["-DSWIGLU_DEBUG"])):
+        if not force and not _stale(so):
+            continue
+        tmp = so + ".%d.tmp" % os.getpid()
+        cmd = [_nvcc(), *NVCC_FLAGS, *extra, "-o", tmp] + [os.path.join(CSRC, f) for f in SOURCES]
+        if verbose:
+            print(" ".join(cmd))
+        jobs.append((subprocess.Popen(cmd), tmp, so, cmd))
+    failed = None
+    for proc, tmp, so, cmd in jobs:
+        if proc.wait() != 0:
+            failed = failed or subprocess.CalledProcessError(proc.returncode, cmd)
+        else:
+            os.replace(tmp, so)
+    if failed is not None:
+        raise failed
     return SO
 
 

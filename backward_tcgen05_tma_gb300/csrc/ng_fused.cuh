@@ -89,6 +89,8 @@ __device__ __forceinline__ NgUnit ng_decode(const NgDynArgs& f, uint32_t u) {
     w.chunk = v / f.ph[1].tiles;
     w.tile = v - w.chunk * f.ph[1].tiles;
   }
+  if (!SWIGLU_CHECK(w.chunk < f.chunks[w.ph] && f.chunks[w.ph] <= NG_MAX_CHUNKS, f.ph[0].err))
+    w.chunk = 0;
   w.kb0 = f.kb_at[w.ph][w.chunk];
   w.nkb = f.kb_at[w.ph][w.chunk + 1] - w.kb0;
   return w;
@@ -196,7 +198,10 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
             const uint32_t bit = 1u << (kb & 31);
             bool ready = mask_idx == (kb >> 5) && (mask_word & bit) != 0u;
             if (!ready) {
-              mask_word = ld_acquire_gpu(f.ready + (kb >> 5));
+              // a k-block outside the mask (debug check) counts as ready: no wait on it
+              mask_word = SWIGLU_CHECK(kb >= 0 && kb < f.ph[0].tiles, err)
+                              ? ld_acquire_gpu(f.ready + (kb >> 5))
+                              : ~0u;
               mask_idx = kb >> 5;
               ready = (mask_word & bit) != 0u;
               // order the acquired A columns before this thread's TMA reads
@@ -378,14 +383,18 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
         const int ph = w.ph, tile = w.tile;
         auto slot = [&](int c) -> float* {
           const int s = ph == 0 ? tile * chunks + c : c * tiles + tile;
-          return a.part + (size_t)s * 128 * NT;
+          return SWIGLU_CHECK(s >= 0 && s < tiles * chunks, err) ? a.part + (size_t)s * 128 * NT
+                                                                  : nullptr;
         };
-        ng_store_partial<NT>(slot(w.chunk), tacc, acce_bar(acc));
+        float* const dst = slot(w.chunk);
+        ng_store_partial<NT>(dst, tacc, acce_bar(acc),
+                             SWIGLU_CHECK_PTR(a.dbg, dst, 128 * NT * 4, err));
         epi_bar_sync();
         if (e == 0) {
           int last = 0;
           __threadfence();  // the 128 threads' partial stores before the count
-          if (!*abort_flag) last = atomicAdd(a.counters + tile, 1) == chunks - 1;
+          if (!*abort_flag)
+            last = SWIGLU_CHECK(tile < tiles, err) && atomicAdd(a.counters + tile, 1) == chunks - 1;
           *last_flag = last;
         }
         epi_bar_sync();
@@ -397,14 +406,15 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
             ng_reduce_store<NT, true, BF16>(a, tile, chunks, part_of);
           else
             ng_reduce_store<NT, false, BF16>(a, tile, chunks, part_of);
-          if (e == 0) a.counters[tile] = 0;  // ready for the next call
+          if (e == 0 && SWIGLU_CHECK(tile < tiles, err)) a.counters[tile] = 0;  // next call
         }
       }
       if (w.ph == 0 && wrote) {
         // publish the tile's A columns to every CTA's down-unit TMA loads
         fence_proxy_async_global();
         epi_bar_sync();
-        if (e == 0 && !(f.inject_unready && w.tile == 0)) {
+        if (e == 0 && !(f.inject_unready && w.tile == 0) &&
+            SWIGLU_CHECK(w.tile < f.ph[0].tiles, err)) {
           __threadfence();
           red_or_release_gpu(f.ready + (w.tile >> 5), 1u << (w.tile & 31));
         }

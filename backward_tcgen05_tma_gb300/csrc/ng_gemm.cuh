@@ -52,7 +52,23 @@ struct NgArgs {
   uint64_t wait_limit_ns;
   int* err;
   float scale = 1.0f;  // gate/up: gate multiplier (SiLU(scale g) u); down: Y = scale y
+#ifdef SWIGLU_DEBUG
+  DbgWin dbg;       // buffers the kernel may touch by plain accesses: out, workspace
+#endif
 };
+
+// out[m, col] = rnd(v) (one element of A or Y); debug builds check the address
+// against the launch's windows.
+template <bool BF16>
+__device__ __forceinline__ void ng_put(const NgArgs& a, int m, int col, float v) {
+  if (BF16) {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out) + (int64_t)m * a.ld_out + col;
+    if (SWIGLU_CHECK_PTR(a.dbg, o, 2, a.err)) *o = __float2bfloat16_rn(v);
+  } else {
+    __half* o = reinterpret_cast<__half*>(a.out) + (int64_t)m * a.ld_out + col;
+    if (SWIGLU_CHECK_PTR(a.dbg, o, 2, a.err)) *o = __float2half_rn(v);
+  }
+}
 
 template <int NT>
 struct NgSmem {
@@ -165,14 +181,7 @@ __device__ __forceinline__ void ng_store_whole(const NgArgs& a, int tile, uint32
     if (row < 64 && j < a.rows) {
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
-        if (n < a.M) {
-          const float o = silu_f32(a.scale * v[n]) * ustage[row * NT + n];
-          if (BF16)
-            reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)n * a.ld_out + j] =
-                __float2bfloat16_rn(o);
-          else
-            reinterpret_cast<__half*>(a.out)[(int64_t)n * a.ld_out + j] = __float2half_rn(o);
-        }
+        if (n < a.M) ng_put<BF16>(a, n, j, silu_f32(a.scale * v[n]) * ustage[row * NT + n]);
       }
     }
     epi_bar_sync();  // ustage is free again
@@ -181,23 +190,18 @@ __device__ __forceinline__ void ng_store_whole(const NgArgs& a, int tile, uint32
     if (d < a.rows) {
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
-        if (n < a.M) {
-          if (BF16)
-            reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)n * a.ld_out + d] =
-                __float2bfloat16_rn(a.scale * v[n]);
-          else
-            reinterpret_cast<__half*>(a.out)[(int64_t)n * a.ld_out + d] =
-                __float2half_rn(a.scale * v[n]);
-        }
+        if (n < a.M) ng_put<BF16>(a, n, d, a.scale * v[n]);
       }
     }
   }
 }
 
-// The accumulator as an fp32 partial tile [128][NT] at ``dst``.  Callers
-// publish it with one release after a barrier over the 128 threads.
+// The accumulator as an fp32 partial tile [128][NT] at ``dst`` (the stores
+// skipped when ``ok`` is false: a debug check failed).  Callers publish it
+// with one release after a barrier over the 128 threads.
 template <int NT>
-__device__ __forceinline__ void ng_store_partial(float* dst, uint32_t tacc, uint32_t acce) {
+__device__ __forceinline__ void ng_store_partial(float* dst, uint32_t tacc, uint32_t acce,
+                                                 bool ok = true) {
   const int row = (threadIdx.x & 96) + (threadIdx.x & 31);
   tc_fence_after();
   float* drow = dst + (size_t)row * NT;
@@ -209,9 +213,10 @@ __device__ __forceinline__ void ng_store_partial(float* dst, uint32_t tacc, uint
     tmem_ld_wait();
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      reinterpret_cast<float4*>(drow + c)[q] =
-          make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                      __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+      if (ok)
+        reinterpret_cast<float4*>(drow + c)[q] =
+            make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                        __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
   }
   tc_fence_before();
   mbar_arrive(acce);  // accumulator free for a later unit
@@ -239,10 +244,13 @@ __device__ __forceinline__ void ng_reduce_store(const NgArgs& a, int tile, int n
       for (int q = 0; q < RB; ++q)
         if (i0 + q < n) {
           const float* pb = part_of(i0 + q);
+          const bool pok = SWIGLU_CHECK_PTR(a.dbg, pb, 128 * NT * 4, a.err);
 #pragma unroll
           for (int k = 0; k < NT / 8; ++k) {
-            vg[q][k] = __ldcg(reinterpret_cast<const float4*>(pb + jr * NT + h * (NT / 2)) + k);
-            vu[q][k] = __ldcg(reinterpret_cast<const float4*>(pb + (64 + jr) * NT + h * (NT / 2)) + k);
+            vg[q][k] = pok ? __ldcg(reinterpret_cast<const float4*>(pb + jr * NT + h * (NT / 2)) + k)
+                           : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            vu[q][k] = pok ? __ldcg(reinterpret_cast<const float4*>(pb + (64 + jr) * NT + h * (NT / 2)) + k)
+                           : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
           }
         }
 #pragma unroll
@@ -261,14 +269,7 @@ __device__ __forceinline__ void ng_reduce_store(const NgArgs& a, int tile, int n
 #pragma unroll
       for (int q = 0; q < NT / 2; ++q) {
         const int m = h * (NT / 2) + q;
-        if (m < a.M) {
-          const float v = silu_f32(a.scale * g[q]) * uu[q];
-          if (BF16)
-            reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)m * a.ld_out + j] =
-                __float2bfloat16_rn(v);
-          else
-            reinterpret_cast<__half*>(a.out)[(int64_t)m * a.ld_out + j] = __float2half_rn(v);
-        }
+        if (m < a.M) ng_put<BF16>(a, m, j, silu_f32(a.scale * g[q]) * uu[q]);
       }
     }
   } else {
@@ -282,9 +283,13 @@ __device__ __forceinline__ void ng_reduce_store(const NgArgs& a, int tile, int n
 #pragma unroll
       for (int q = 0; q < RB; ++q)
         if (i0 + q < n) {
-          const float* pb = part_of(i0 + q) + e * NT;
+          const float* pt = part_of(i0 + q);
+          const bool pok = SWIGLU_CHECK_PTR(a.dbg, pt, 128 * NT * 4, a.err);
+          const float* pb = pt + e * NT;
 #pragma unroll
-          for (int k = 0; k < NT / 4; ++k) v[q][k] = __ldcg(reinterpret_cast<const float4*>(pb) + k);
+          for (int k = 0; k < NT / 4; ++k)
+            v[q][k] = pok ? __ldcg(reinterpret_cast<const float4*>(pb) + k)
+                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
 #pragma unroll
       for (int q = 0; q < RB; ++q)
@@ -299,14 +304,7 @@ __device__ __forceinline__ void ng_reduce_store(const NgArgs& a, int tile, int n
     if (d < a.rows) {
 #pragma unroll
       for (int q = 0; q < NT; ++q) {
-        if (q < a.M) {
-          if (BF16)
-            reinterpret_cast<__nv_bfloat16*>(a.out)[(int64_t)q * a.ld_out + d] =
-                __float2bfloat16_rn(a.scale * y[q]);
-          else
-            reinterpret_cast<__half*>(a.out)[(int64_t)q * a.ld_out + d] =
-                __float2half_rn(a.scale * y[q]);
-        }
+        if (q < a.M) ng_put<BF16>(a, q, d, a.scale * y[q]);
       }
     }
   }
@@ -326,7 +324,10 @@ __device__ __forceinline__ bool ng_epilogue_segment(const NgArgs& a, int tile, b
     ng_store_whole<NT, GATE_UP, BF16>(a, tile, tacc, acce, ustage);
     return true;
   }
-  ng_store_partial<NT>(a.part + ((size_t)blockIdx.x * a.seg_max + seg) * 128 * NT, tacc, acce);
+  float* const dst = a.part + ((size_t)blockIdx.x * a.seg_max + seg) * 128 * NT;
+  ng_store_partial<NT>(dst, tacc, acce,
+                       SWIGLU_CHECK(seg < a.seg_max, a.err) &&
+                           SWIGLU_CHECK_PTR(a.dbg, dst, 128 * NT * 4, a.err));
   // CTAs sharing this tile: owners of its first and last k-block
   const int c_first = ng_owner((int64_t)tile * a.kb_tile, total, ctas);
   const int c_last = ng_owner((int64_t)(tile + 1) * a.kb_tile - 1, total, ctas);
@@ -336,7 +337,8 @@ __device__ __forceinline__ bool ng_epilogue_segment(const NgArgs& a, int tile, b
   if (e == 0) {
     int last = 0;
     __threadfence();  // the 128 threads' partial stores before the count
-    if (!*abort_flag) last = atomicAdd(a.counters + tile, 1) == nparts - 1;
+    if (!*abort_flag)
+      last = SWIGLU_CHECK(tile < a.tiles, a.err) && atomicAdd(a.counters + tile, 1) == nparts - 1;
     *last_flag = last;
   }
   epi_bar_sync();
@@ -347,9 +349,11 @@ __device__ __forceinline__ bool ng_epilogue_segment(const NgArgs& a, int tile, b
     ng_reduce_store<NT, GATE_UP, BF16>(a, tile, nparts, [&](int i) -> const float* {
       const int c = c_first + i;
       const int j = tile - (int)(ng_start(c, total, ctas) / a.kb_tile);
-      return a.part + ((size_t)c * a.seg_max + j) * 128 * NT;
+      return SWIGLU_CHECK(j >= 0 && j < a.seg_max, a.err)
+                 ? a.part + ((size_t)c * a.seg_max + j) * 128 * NT
+                 : nullptr;
     });
-    if (e == 0) a.counters[tile] = 0;  // ready for the next call
+    if (e == 0 && SWIGLU_CHECK(tile < a.tiles, a.err)) a.counters[tile] = 0;  // next call
   }
   return last != 0;
 }
@@ -384,7 +388,8 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
 
   if (blockIdx.x == 0 && a.clear_err && threadIdx.x == 0) *a.err = 0;
   if (!a.dependent) {
-    if (blockIdx.x == 0)
+    if (blockIdx.x == 0 &&
+        SWIGLU_CHECK_PTR(a.dbg, a.zero_ptr, 4 * (int64_t)a.zero_count, a.err))
       for (int i = threadIdx.x; i < a.zero_count; i += blockDim.x) a.zero_ptr[i] = 0;
     pdl_launch_dependents();  // the down kernel may begin its prologue
   }
@@ -455,7 +460,8 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
           }
         }
         pdl_wait();
-        if (blockIdx.x == 0)
+        if (blockIdx.x == 0 &&
+            SWIGLU_CHECK_PTR(a.dbg, a.zero_ptr, 4 * (int64_t)a.zero_count, a.err))
           for (int i = 0; i < a.zero_count; ++i) a.zero_ptr[i] = 0;
         for (int i = 0; i < pending_x; ++i)
           tma_load_2d(sbase + i * L::STAGE_BYTES + L::W_BYTES, &tmX, full_bar(i), pending_k0[i], 0);

@@ -15,9 +15,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "sm103_ptx.cuh"
+
 namespace swiglu {
 
 constexpr int SG_BM = 64, SG_BN = 64, SG_BK = 16, SG_THREADS = 256;
+
+// Debug builds: the error word and the windows (operands, outputs) every
+// element access is checked against; empty in release builds.
+struct SimtCheck {
+#ifdef SWIGLU_DEBUG
+  int* err;
+  DbgWin win;
+#endif
+};
+
+// p[0], or 0 when a debug check rejects the address
+__device__ __forceinline__ float simt_ld(const float* p, const SimtCheck& chk) {
+  return SWIGLU_CHECK_PTR(chk.win, p, 4, chk.err) ? *p : 0.0f;
+}
 
 struct SimtOperand {
   const float* p;
@@ -31,9 +47,10 @@ struct SimtEpiStore {
   int64_t ld;
   float scale = 1.0f;   // out = scale * acc ...
   int accumulate = 0;   // ... or, if nonzero, out + scale * acc
-  __device__ __forceinline__ void apply(int m, int n, float acc, float) const {
+  __device__ __forceinline__ void apply(int m, int n, float acc, float,
+                                        const SimtCheck& chk) const {
     float* o = out + (int64_t)m * ld + n;
-    *o = accumulate ? *o + scale * acc : scale * acc;
+    if (SWIGLU_CHECK_PTR(chk.win, o, 4, chk.err)) *o = accumulate ? *o + scale * acc : scale * acc;
   }
 };
 
@@ -47,13 +64,17 @@ struct SimtEpiSwiGLU {
   float* a;
   int64_t ld_a;
   float gate_mul = 1.0f;
-  __device__ __forceinline__ void apply(int m, int n, float acc, float uv) const {
+  __device__ __forceinline__ void apply(int m, int n, float acc, float uv,
+                                        const SimtCheck& chk) const {
     const float gv = gate_mul * acc;
     if (g != nullptr) {
-      g[(int64_t)m * ld_gu + n] = gv;
-      u[(int64_t)m * ld_gu + n] = uv;
+      float* og = g + (int64_t)m * ld_gu + n;
+      float* ou = u + (int64_t)m * ld_gu + n;
+      if (SWIGLU_CHECK_PTR(chk.win, og, 4, chk.err)) *og = gv;
+      if (SWIGLU_CHECK_PTR(chk.win, ou, 4, chk.err)) *ou = uv;
     }
-    a[(int64_t)m * ld_a + n] = gv / (1.0f + expf(-gv)) * uv;
+    float* oa = a + (int64_t)m * ld_a + n;
+    if (SWIGLU_CHECK_PTR(chk.win, oa, 4, chk.err)) *oa = gv / (1.0f + expf(-gv)) * uv;
   }
 };
 
@@ -65,8 +86,12 @@ struct SimtEpiDSwiGLU {
   float* u;
   int64_t ld;
   float gate_mul = 1.0f, down_mul = 1.0f;
-  __device__ __forceinline__ void apply(int m, int n, float acc, float) const {
+  __device__ __forceinline__ void apply(int m, int n, float acc, float,
+                                        const SimtCheck& chk) const {
     const int64_t o = (int64_t)m * ld + n;
+    if (!(SWIGLU_CHECK_PTR(chk.win, g + o, 4, chk.err) &&
+          SWIGLU_CHECK_PTR(chk.win, u + o, 4, chk.err)))
+      return;
     const float da = down_mul * acc;
     const float gv = g[o], uv = u[o];
     const float s = 1.0f / (1.0f + expf(-gv));
@@ -79,7 +104,8 @@ struct SimtEpiDSwiGLU {
 // both sums (used by the gate/up GEMM: B = Wg rows, B2 = Wu rows).
 template <bool DUAL, class Epi>
 __global__ void __launch_bounds__(SG_THREADS)
-    simt_gemm_kernel(SimtOperand A, SimtOperand B, SimtOperand B2, int M, int N, int K, Epi epi) {
+    simt_gemm_kernel(SimtOperand A, SimtOperand B, SimtOperand B2, int M, int N, int K, Epi epi,
+                     SimtCheck chk) {
   __shared__ float As[SG_BK][SG_BM + 4];
   __shared__ float Bs[SG_BK][SG_BN + 4];
   __shared__ float B2s[DUAL ? SG_BK : 1][SG_BN + 4];
@@ -94,10 +120,14 @@ __global__ void __launch_bounds__(SG_THREADS)
       const int idx = threadIdx.x + i * SG_THREADS;
       const int r = idx / SG_BK, kk = idx % SG_BK;
       const int m = m0 + r, n = n0 + r, k = k0 + kk;
-      As[kk][r] = (m < M && k < K) ? A.p[(int64_t)m * A.s_row + (int64_t)k * A.s_k] : 0.0f;
-      Bs[kk][r] = (n < N && k < K) ? B.p[(int64_t)n * B.s_row + (int64_t)k * B.s_k] : 0.0f;
+      As[kk][r] = (m < M && k < K) ? simt_ld(A.p + (int64_t)m * A.s_row + (int64_t)k * A.s_k, chk)
+                                   : 0.0f;
+      Bs[kk][r] = (n < N && k < K) ? simt_ld(B.p + (int64_t)n * B.s_row + (int64_t)k * B.s_k, chk)
+                                   : 0.0f;
       if (DUAL)
-        B2s[kk][r] = (n < N && k < K) ? B2.p[(int64_t)n * B2.s_row + (int64_t)k * B2.s_k] : 0.0f;
+        B2s[kk][r] = (n < N && k < K)
+                         ? simt_ld(B2.p + (int64_t)n * B2.s_row + (int64_t)k * B2.s_k, chk)
+                         : 0.0f;
     }
     __syncthreads();
 #pragma unroll
@@ -124,7 +154,7 @@ __global__ void __launch_bounds__(SG_THREADS)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int m = m0 + ty * 4 + i, n = n0 + tx * 4 + j;
-      if (m < M && n < N) epi.apply(m, n, acc[i][j], acc2[i][j]);
+      if (m < M && n < N) epi.apply(m, n, acc[i][j], acc2[i][j], chk);
     }
 }
 

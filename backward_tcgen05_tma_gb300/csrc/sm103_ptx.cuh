@@ -10,7 +10,43 @@
 namespace swiglu {
 
 // Error codes stored in the workspace error word (0 = no error).
-enum : int { DEV_ERR_NONE = 0, DEV_ERR_TIMEOUT = 6 };
+enum : int { DEV_ERR_NONE = 0, DEV_ERR_TIMEOUT = 6, DEV_ERR_BOUNDS = 7 };
+
+// Debug builds (compiled with -DSWIGLU_DEBUG): index checks on every plain
+// (non-TMA) global access.  Each launch carries up to DBG_WINS byte windows,
+// the buffers it may touch; an access outside all of them, or an index
+// outside its table, records DEV_ERR_BOUNDS in the error word and is skipped,
+// so the kernel finishes and the host reads the error (no trap, no fault).
+// TMA accesses need no check: the tensor map clips them to the tensor.  In
+// release builds every check is the constant `true` and compiles away.
+constexpr int DBG_WINS = 4;
+struct DbgWin {
+  uint64_t lo[DBG_WINS];  // window i = [lo[i], hi[i]); empty when lo == hi
+  uint64_t hi[DBG_WINS];
+};
+
+#ifdef SWIGLU_DEBUG
+__device__ __noinline__ bool dbg_fail(int* err) {
+  atomicCAS(err, DEV_ERR_NONE, DEV_ERR_BOUNDS);
+  return false;
+}
+__device__ __forceinline__ bool dbg_in(const DbgWin& w, const void* p, int64_t bytes) {
+  const uint64_t a = reinterpret_cast<uint64_t>(p);
+  bool in = false;
+#pragma unroll
+  for (int i = 0; i < DBG_WINS; ++i)
+    in |= bytes >= 0 && a >= w.lo[i] && a + (uint64_t)bytes <= w.hi[i] && w.lo[i] < w.hi[i];
+  return in;
+}
+// cond must hold; else record the error and return false (skip the access)
+#define SWIGLU_CHECK(cond, err) ((cond) ? true : ::swiglu::dbg_fail(err))
+// [p, p + bytes) must lie inside one of the launch's windows
+#define SWIGLU_CHECK_PTR(win, p, bytes, err) \
+  SWIGLU_CHECK(::swiglu::dbg_in((win), (p), (bytes)), (err))
+#else
+#define SWIGLU_CHECK(cond, err) true
+#define SWIGLU_CHECK_PTR(win, p, bytes, err) true
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -17,7 +17,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "../../include/swiglu_mlp.h"
@@ -38,6 +40,52 @@ constexpr int TC_BN = 256;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 
 swiglu_status cuda_status(cudaError_t e);
+
+// Debug builds (SWIGLU_DEBUG): the buffers (base, bytes) a launch may touch
+// with plain loads and stores, its output first; the kernels check every
+// such access against them.  Release builds carry no windows.
+using Win = std::pair<const void*, size_t>;
+
+// Test hook (swiglu_mlp_debug_narrow_once): halve the next launch's first
+// window, its output buffer.
+std::atomic<int> g_narrow_once{0};
+
+#ifdef SWIGLU_DEBUG
+DbgWin make_windows(std::initializer_list<Win> wins) {
+  DbgWin w = {};
+  int i = 0;
+  for (const Win& b : wins) {
+    if (i == DBG_WINS) break;
+    w.lo[i] = reinterpret_cast<uint64_t>(b.first);
+    w.hi[i] = w.lo[i] + b.second;
+    ++i;
+  }
+  if (g_narrow_once.exchange(0)) w.hi[0] = w.lo[0] + (w.hi[0] - w.lo[0]) / 2;
+  return w;
+}
+#endif
+
+template <class T>
+void set_windows(T& args, std::initializer_list<Win> wins) {
+#ifdef SWIGLU_DEBUG
+  args.dbg = make_windows(wins);
+#else
+  (void)args;
+  (void)wins;
+#endif
+}
+
+SimtCheck simt_check(int* err, std::initializer_list<Win> wins) {
+  SimtCheck c;
+#ifdef SWIGLU_DEBUG
+  c.err = err;
+  c.win = make_windows(wins);
+#else
+  (void)err;
+  (void)wins;
+#endif
+  return c;
+}
 
 // The multiplier / accumulation options of the _ex entry points (see the
 // header); {1, 1, 0} is the standard MLP with gradients overwritten.
@@ -405,10 +453,12 @@ cudaError_t launch_gemm(bool pairs, int kid, const CUtensorMap& ta, const CUtens
 
 template <bool DUAL, class Epi>
 cudaError_t launch_simt(int kid, SimtOperand A, SimtOperand B, SimtOperand B2, int64_t M,
-                        int64_t N, int64_t K, const Epi& epi, cudaStream_t st) {
+                        int64_t N, int64_t K, const Epi& epi, const SimtCheck& chk,
+                        cudaStream_t st) {
   dim3 grid((unsigned)((N + SG_BN - 1) / SG_BN), (unsigned)((M + SG_BM - 1) / SG_BM));
   ProfScope prof(kid, st);
-  simt_gemm_kernel<DUAL, Epi><<<grid, SG_THREADS, 0, st>>>(A, B, B2, (int)M, (int)N, (int)K, epi);
+  simt_gemm_kernel<DUAL, Epi>
+      <<<grid, SG_THREADS, 0, st>>>(A, B, B2, (int)M, (int)N, (int)K, epi, chk);
   g_last_launches.fetch_add(1);
   return cudaGetLastError();
 }
@@ -575,7 +625,7 @@ cudaError_t launch_ng(int kid, const CUtensorMap& tw, const CUtensorMap& tx, NgA
 template <int NT, bool BF16>
 swiglu_status ng_forward_nt(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
                             int64_t M, int64_t D, int64_t H, const NgPlan& p, char* ws,
-                            const Opts& o, cudaStream_t st) {
+                            size_t ws_cap, const Opts& o, cudaStream_t st) {
   int* err = reinterpret_cast<int*>(ws);
   int* counters = reinterpret_cast<int*>(ws + WS_HEADER);
   float* part = reinterpret_cast<float*>(ws + WS_HEADER + p.counter_bytes);
@@ -586,6 +636,7 @@ swiglu_status ng_forward_nt(const void* X, const void* Wgu, const void* Wd, void
   NgArgs a1{(int)M, (int)H, p.kb1, p.t1, 0, 0, part, counters, counters + p.t1, p.t2, 1, 0, 0,
             A, H, wl, err};
   a1.scale = o.gm;
+  set_windows(a1, {{A, (size_t)(M * H * 2)}, {ws, ws_cap}});
   if (launch_ng<NT, true, BF16>(K_NG_GATE_UP, tw, tx, a1, st) != cudaSuccess)
     return SWIGLU_ERR_CUDA;
   if (!map_kmajor(&tw, BF16, Wd, H, D, H, 128) || !map_kmajor(&tx, BF16, A, H, M, H, NT))
@@ -593,6 +644,7 @@ swiglu_status ng_forward_nt(const void* X, const void* Wgu, const void* Wd, void
   NgArgs a2{(int)M, (int)D, p.kb2, p.t2, 0, 0, part, counters + p.t1, counters, p.t1, 0, 1, 0,
             Y, D, wl, err};
   a2.scale = o.dm;
+  set_windows(a2, {{Y, (size_t)(M * D * 2)}, {ws, ws_cap}});
   return cuda_status(launch_ng<NT, false, BF16>(K_NG_DOWN, tw, tx, a2, st));
 }
 
@@ -606,7 +658,7 @@ constexpr size_t NG_NEXT_OFFSET = 192;  // the fused kernel's work-queue counter
 template <int NT, bool BF16>
 swiglu_status ng_forward_fused(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
                                int64_t M, int64_t D, int64_t H, const NgPlan& p, char* ws,
-                               const Opts& o, cudaStream_t st) {
+                               size_t ws_cap, const Opts& o, cudaStream_t st) {
   auto kern = ng_fused_kernel<NT, BF16>;
   constexpr int smem = NgDynSmem<NT>::DYN_BYTES;
   {
@@ -648,6 +700,8 @@ swiglu_status ng_forward_fused(const void* X, const void* Wgu, const void* Wd, v
                    0, Y, D, wl, err};
   f.ph[0].scale = o.gm;
   f.ph[1].scale = o.dm;
+  set_windows(f.ph[0], {{A, (size_t)(M * H * 2)}, {ws, ws_cap}});
+  set_windows(f.ph[1], {{Y, (size_t)(M * D * 2)}, {ws, ws_cap}});
   ProfScope prof(K_NG_FUSED, st);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)d.grid);
@@ -669,9 +723,9 @@ swiglu_status ng_forward_t(const void* X, const void* Wgu, const void* Wd, void*
                            size_t ws_cap, const Opts& o, cudaStream_t st) {
   const int mode = g_ng_fused.load();
   if ((mode == 2 || (mode == 1 && NT == 64)) && ng_fused_bytes(p) <= ws_cap)
-    return ng_forward_fused<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, o, st);
+    return ng_forward_fused<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, o, st);
   if (ng_two_bytes(p) > ws_cap) return SWIGLU_ERR_UNSUPPORTED;
-  return ng_forward_nt<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, o, st);
+  return ng_forward_nt<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, o, st);
 }
 
 template <bool BF16>
@@ -787,6 +841,9 @@ swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y
       !encode_gateup(&tw, BF16, Wgu, D, H, TC_BN / 2, pairs1 ? 1 : 2))
     return SWIGLU_ERR_CUDA;
   TcShape s1 = make_shape(M, H, D, TC_BN / 2, err, pairs1, cap);
+  // training: G, U and A are column ranges of the saved rows; no-grad: A alone
+  set_windows(s1, {{G != nullptr ? G : A, (size_t)(M * (G != nullptr ? ld_gu : ld_a) * 2)},
+                   {err, ws_bytes}});
   EpiSwiGLU::Params p1{G, U, ld_gu, A, ld_a, o.gm};
   cudaError_t e = launch_gemm<LOAD_KMAJOR, LOAD_GATEUP, BF16, EpiSwiGLU>(
       pairs1, G != nullptr ? K_GATE_UP : K_GATE_UP_NOGRAD, tx, tw, s1, p1, st);
@@ -798,6 +855,7 @@ swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y
       !map_kmajor(&twd, BF16, Wd, H, D, H, pairs2 ? 128 : TC_BN))
     return SWIGLU_ERR_CUDA;
   TcShape s2 = make_shape(M, D, H, TC_BN, err, pairs2, cap);
+  set_windows(s2, {{Y, (size_t)(M * D * 2)}, {err, ws_bytes}});
   EpiStore::Params p2{Y, D, o.dm, 0};
   return cuda_status(launch_gemm<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore>(
       pairs2, G != nullptr ? K_DOWN : K_DOWN_NOGRAD, ta, twd, s2, p2, st));
@@ -822,6 +880,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   {
     const bool pairs = use_pairs(D, H, TC_BN, M);
     TcShape s = make_shape(D, H, M, TC_BN, err, pairs, cap);
+    set_windows(s, {{dWd, (size_t)(D * H * 2)}, {err, ws_bytes}});
     EpiStore::Params p{dWd, H, o.dm, o.acc};
     e = launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWD, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
@@ -832,6 +891,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   {
     const bool pairs = use_pairs(M, H, TC_BN, D);
     TcShape s = make_shape(M, H, D, TC_BN, err, pairs, cap);
+    set_windows(s, {{saved, (size_t)(M * ld * 2)}, {err, ws_bytes}});
     EpiDSwiGLU::Params p{G, U, ld, o.gm, o.dm};
     // a short contraction leaves the epilogue the bound: direct G/U loads
     e = D <= 2048 ? launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLUT<true>>(
@@ -846,6 +906,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   {
     const bool pairs = use_pairs(2 * H, D, TC_BN, M);
     TcShape s = make_shape(2 * H, D, M, TC_BN, err, pairs, cap);
+    set_windows(s, {{dWgu, (size_t)(2 * H * D * 2)}, {err, ws_bytes}});
     EpiStore::Params p{dWgu, D, 1.0f, o.acc};
     e = launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWGU, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
@@ -856,6 +917,7 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
   {
     const bool pairs = use_pairs(M, D, TC_BN, 2 * H);
     TcShape s = make_shape(M, D, 2 * H, TC_BN, err, pairs, cap);
+    set_windows(s, {{dX, (size_t)(M * D * 2)}, {err, ws_bytes}});
     EpiStore::Params p{dX, D, 1.0f, 0};
     e = launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DX, m1, m2, s, p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
@@ -868,37 +930,53 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
 // ---------------------------------------------------------------------------
 swiglu_status simt_forward(const float* X, const float* Wgu, const float* Wd, float* Y, float* G,
                            float* U, int64_t ld_gu, float* A, int64_t ld_a, int64_t M, int64_t D,
-                           int64_t H, const Opts& o, cudaStream_t st) {
+                           int64_t H, int* err, const Opts& o, cudaStream_t st) {
+  // training: G, U and A are column ranges of the saved rows; no-grad: A alone
+  const Win out{G != nullptr ? (const void*)G : (const void*)A,
+                (size_t)(M * (G != nullptr ? ld_gu : ld_a) * 4)};
+  const Win x_w{X, (size_t)(M * D * 4)}, wgu_w{Wgu, (size_t)(2 * H * D * 4)},
+      wd_w{Wd, (size_t)(D * H * 4)}, y_w{Y, (size_t)(M * D * 4)};
   SimtOperand x{X, D, 1}, wg{Wgu, D, 1}, wu{Wgu + H * D, D, 1};
-  cudaError_t e = launch_simt<true>(K_SIMT_GATE_UP, x, wg, wu, M, H, D, SimtEpiSwiGLU{G, U, ld_gu, A, ld_a, o.gm}, st);
+  cudaError_t e = launch_simt<true>(K_SIMT_GATE_UP, x, wg, wu, M, H, D,
+                                    SimtEpiSwiGLU{G, U, ld_gu, A, ld_a, o.gm},
+                                    simt_check(err, {out, x_w, wgu_w}), st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   SimtOperand a{A, ld_a, 1}, wd{Wd, H, 1};
-  return cuda_status(launch_simt<false>(K_SIMT_DOWN, a, wd, wd, M, D, H, SimtEpiStore{Y, D, o.dm, 0}, st));
+  return cuda_status(launch_simt<false>(K_SIMT_DOWN, a, wd, wd, M, D, H,
+                                        SimtEpiStore{Y, D, o.dm, 0},
+                                        simt_check(err, {y_w, out, wd_w}), st));
 }
 
 swiglu_status simt_backward(const float* dY, const float* X, const float* Wgu, const float* Wd,
                             float* saved, float* dX, float* dWgu, float* dWd, int64_t M,
-                            int64_t D, int64_t H, const Opts& o, cudaStream_t st) {
+                            int64_t D, int64_t H, int* err, const Opts& o, cudaStream_t st) {
   const int64_t ld = 3 * H;
   float* G = saved;
   float* U = saved + H;
   float* A = saved + 2 * H;
+  const Win dy_w{dY, (size_t)(M * D * 4)}, x_w{X, (size_t)(M * D * 4)},
+      wgu_w{Wgu, (size_t)(2 * H * D * 4)}, wd_w{Wd, (size_t)(D * H * 4)},
+      sv_w{saved, (size_t)(M * ld * 4)};
   cudaError_t e;
   // dA = dY Wd: A(m, d) = dY[m, d]; B(j, d) = Wd[d, j]
   e = launch_simt<false>(K_SIMT_DGU, SimtOperand{dY, D, 1}, SimtOperand{Wd, 1, H}, SimtOperand{Wd, 1, H}, M,
-                         H, D, SimtEpiDSwiGLU{G, U, ld, o.gm, o.dm}, st);
+                         H, D, SimtEpiDSwiGLU{G, U, ld, o.gm, o.dm},
+                         simt_check(err, {sv_w, dy_w, wd_w}), st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   // dWd[d, j] = sum_m dY[m, d] A[m, j]
   e = launch_simt<false>(K_SIMT_DWD, SimtOperand{dY, 1, D}, SimtOperand{A, 1, ld}, SimtOperand{A, 1, ld}, D,
-                         H, M, SimtEpiStore{dWd, H, o.dm, o.acc}, st);
+                         H, M, SimtEpiStore{dWd, H, o.dm, o.acc},
+                         simt_check(err, {Win{dWd, (size_t)(D * H * 4)}, dy_w, sv_w}), st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   // dWgu[j', d] = sum_m dGU[m, j'] X[m, d]
   e = launch_simt<false>(K_SIMT_DWGU, SimtOperand{G, 1, ld}, SimtOperand{X, 1, D}, SimtOperand{X, 1, D}, 2 * H,
-                         D, M, SimtEpiStore{dWgu, D, 1.0f, o.acc}, st);
+                         D, M, SimtEpiStore{dWgu, D, 1.0f, o.acc},
+                         simt_check(err, {Win{dWgu, (size_t)(2 * H * D * 4)}, sv_w, x_w}), st);
   if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   // dX[m, d] = sum_j' dGU[m, j'] Wgu[j', d]
   e = launch_simt<false>(K_SIMT_DX, SimtOperand{G, ld, 1}, SimtOperand{Wgu, 1, D}, SimtOperand{Wgu, 1, D}, M,
-                         D, 2 * H, SimtEpiStore{dX, D, 1.0f, 0}, st);
+                         D, 2 * H, SimtEpiStore{dX, D, 1.0f, 0},
+                         simt_check(err, {Win{dX, (size_t)(M * D * 4)}, sv_w, wgu_w}), st);
   return cuda_status(e);
 }
 
@@ -963,7 +1041,7 @@ swiglu_status swiglu_mlp_fwd_ex(const void* X, const void* Wgu, const void* Wd, 
       return tc_forward<false>(X, Wgu, Wd, Y, G, U, 3 * H, A, 3 * H, M, D, H, err, ws_bytes, o, s);
     default:
       return simt_forward((const float*)X, (const float*)Wgu, (const float*)Wd, (float*)Y,
-                          (float*)G, (float*)U, 3 * H, (float*)A, 3 * H, M, D, H, o, s);
+                          (float*)G, (float*)U, 3 * H, (float*)A, 3 * H, M, D, H, err, o, s);
   }
 }
 
@@ -1001,7 +1079,7 @@ swiglu_status swiglu_mlp_fwd_nograd_ex(const void* X, const void* Wgu, const voi
       return tc_forward<false>(X, Wgu, Wd, Y, nullptr, nullptr, 0, A, H, M, D, H, err, ws_bytes, o, s);
     default:
       return simt_forward((const float*)X, (const float*)Wgu, (const float*)Wd, (float*)Y,
-                          nullptr, nullptr, 0, (float*)A, H, M, D, H, o, s);
+                          nullptr, nullptr, 0, (float*)A, H, M, D, H, err, o, s);
   }
 }
 
@@ -1063,7 +1141,7 @@ swiglu_status swiglu_mlp_bwd_ex(const void* dY, const void* X, const void* Wgu, 
     default:
       return simt_backward((const float*)dY, (const float*)X, (const float*)Wgu,
                            (const float*)Wd, (float*)saved, (float*)dX, (float*)dWgu,
-                           (float*)dWd, M, D, H, o, s);
+                           (float*)dWd, M, D, H, err, o, s);
   }
 }
 
@@ -1160,7 +1238,18 @@ swiglu_status swiglu_mlp_query_error(const void* ws, void* stream) {
     return SWIGLU_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return SWIGLU_ERR_CUDA;
   if (host == DEV_ERR_TIMEOUT) return SWIGLU_ERR_DEVICE_TIMEOUT;
+  if (host == DEV_ERR_BOUNDS) return SWIGLU_ERR_DEVICE_BOUNDS;
   return host == 0 ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
+
+void swiglu_mlp_debug_narrow_once(int on) { g_narrow_once.store(on ? 1 : 0); }
+
+int swiglu_mlp_debug_build(void) {
+#ifdef SWIGLU_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 const char* swiglu_status_string(swiglu_status status) {
@@ -1172,6 +1261,7 @@ const char* swiglu_status_string(swiglu_status status) {
     case SWIGLU_ERR_WORKSPACE: return "workspace missing or too small";
     case SWIGLU_ERR_CUDA: return "CUDA error";
     case SWIGLU_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    case SWIGLU_ERR_DEVICE_BOUNDS: return "device index check failed (debug build)";
     default: return "unknown status";
   }
 }

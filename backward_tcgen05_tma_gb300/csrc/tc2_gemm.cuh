@@ -251,6 +251,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // this CTA's 128 rows of the partial tile -> its slot, in TMEM order
         float4* slot = reinterpret_cast<float4*>(
             s.part + ((size_t)blockIdx.x * s.seg_max + seg) * (size_t)(TC_BM * BN));
+        const bool slot_ok = SWIGLU_CHECK(seg < s.seg_max, s.err) &&
+                             SWIGLU_CHECK_PTR(s.dbg, slot, (int64_t)TC_BM * BN * 4, s.err);
 #pragma unroll 1
         for (int c = half * CH; c < (half + 1) * CH; ++c) {
           uint32_t r[32];
@@ -258,9 +260,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int g = 0; g < 8; ++g)
-            slot[((c * 4 + quarter) * 8 + g) * 32 + lane] =
-                make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                            __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+            if (slot_ok)
+              slot[((c * 4 + quarter) * 8 + g) * 32 + lane] =
+                  make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                              __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
         }
         __threadfence();
         ++seg;
@@ -270,7 +273,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_epi_bar();
         if (e == 0) {
           int last = 0;
-          if (!*abort_flag) last = atomicAdd(s.counters + 2 * tile + rank, 1) == c_last - c_first;
+          if (!*abort_flag)
+            last = SWIGLU_CHECK(2 * tile + rank < 2 * s.sk_tiles, s.err) &&
+                   atomicAdd(s.counters + 2 * tile + rank, 1) == c_last - c_first;
           *last_flag = last;
         }
         tc_epi_bar();
@@ -294,9 +299,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int j = tile - (int)(sk_start(pc, sk_total, ncl) / s.k_blocks);
                 const float4* ps = reinterpret_cast<const float4*>(
                     s.part + ((size_t)(2 * pc + rank) * s.seg_max + j) * (size_t)(TC_BM * BN));
+                const bool ps_ok =
+                    SWIGLU_CHECK(j >= 0 && j < s.seg_max, s.err) &&
+                    SWIGLU_CHECK_PTR(s.dbg, ps, (int64_t)TC_BM * BN * 4, s.err);
                 float4 v[8];
 #pragma unroll
-                for (int g = 0; g < 8; ++g) v[g] = __ldcg(ps + ((c * 4 + quarter) * 8 + g) * 32 + lane);
+                for (int g = 0; g < 8; ++g)
+                  v[g] = ps_ok ? __ldcg(ps + ((c * 4 + quarter) * 8 + g) * 32 + lane)
+                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
                   sum[4 * g] += v[g].x;
@@ -312,7 +322,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tmem_st_32x32b_x32(tacc + c * 32, w);
           }
           tmem_st_wait();
-          if (e == 0) s.counters[2 * tile + rank] = 0;  // ready for the next launch
+          // ready for the next launch
+          if (e == 0 && SWIGLU_CHECK(2 * tile + rank < 2 * s.sk_tiles, s.err))
+            s.counters[2 * tile + rank] = 0;
           tc_fence_before();
           tc_epi_bar();
           tc_fence_after();

@@ -57,6 +57,9 @@ struct TcShape {
   int seg_max;     // partial slots per CTA
   float* part;     // [gridDim.x * seg_max][128 * BN] fp32 in TMEM order
   int* counters;   // [sk_tiles], zero at launch; each reducer re-zeroes its own
+#ifdef SWIGLU_DEBUG
+  DbgWin dbg;      // buffers the epilogue may touch: its output(s) and the workspace
+#endif
 };
 
 // Stream-K partition of `total` shared k-blocks: CTA c owns
@@ -171,6 +174,28 @@ struct Pack<false> {
 // conflicts.  row_ptr(r) is row r's destination for this chunk (or nullptr
 // when the row is outside the matrix); chunk_ok(q) says whether 8-column
 // group q lies inside it.
+// Debug builds: row_ptr wrapped so that the bytes each row access touches
+// (the 16-byte groups chunk_ok admits, a prefix of the row's 64) are checked
+// against the launch's windows; a row that fails is skipped.  Release
+// builds: row_ptr itself.
+template <class RowPtr, class ChunkOk>
+__device__ __forceinline__ auto checked_rows(const TcShape& s, RowPtr row_ptr, ChunkOk chunk_ok) {
+#ifdef SWIGLU_DEBUG
+  return [=, &s](int r) -> decltype(row_ptr(0)) {
+    auto p = row_ptr(r);
+    if (p == nullptr) return p;
+    int nq = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) nq += chunk_ok(q) ? 1 : 0;
+    return nq == 0 || SWIGLU_CHECK_PTR(s.dbg, p, nq * 16, s.err) ? p : nullptr;
+  };
+#else
+  (void)s;
+  (void)chunk_ok;
+  return row_ptr;
+#endif
+}
+
 template <class RowPtr, class ChunkOk>
 __device__ __forceinline__ void warp_store_tile(uint8_t* buf, const uint32_t (&v)[16], int lane,
                                                 RowPtr row_ptr, ChunkOk chunk_ok) {
@@ -268,10 +293,11 @@ struct EpiStore {
                        : nullptr;
       };
       auto ok = [&](int q) { return nc + q * 8 + 8 <= s.N; };
+      const auto crows = checked_rows(s, rows, ok);
       uint4 old[4];
       if (p.accumulate) {
         uint4 w[4];
-        warp_load_issue(w, lane, rows, ok);
+        warp_load_issue(w, lane, crows, ok);
         warp_load_finish(buf, w, lane, old);
       }
       uint32_t r[32];
@@ -289,7 +315,7 @@ struct EpiStore {
         }
         v[i] = P::two(a0, a1);
       }
-      warp_store_tile(buf, v, lane, rows, ok);
+      warp_store_tile(buf, v, lane, crows, ok);
     }
   }
 };
@@ -343,10 +369,10 @@ struct EpiSwiGLU {
                          : nullptr;
         };
       };
-      warp_store_tile(buf, va, lane, dst(p.a, p.ld_a), ok);
+      warp_store_tile(buf, va, lane, checked_rows(s, dst(p.a, p.ld_a), ok), ok);
       if (keep_gu) {
-        warp_store_tile(buf, vg, lane, dst(p.g, p.ld_gu), ok);
-        warp_store_tile(buf, vu, lane, dst(p.u, p.ld_gu), ok);
+        warp_store_tile(buf, vg, lane, checked_rows(s, dst(p.g, p.ld_gu), ok), ok);
+        warp_store_tile(buf, vu, lane, checked_rows(s, dst(p.u, p.ld_gu), ok), ok);
       }
     }
   }
@@ -400,9 +426,12 @@ struct EpiDSwiGLUT {
     auto load_row = [&](uint4 (&w)[4], void* base, int jc) {  // DIRECT: this thread's row
       const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(base) +
                                                         (int64_t)mrow * p.ld + jc);
+      const int ncols = min(32, s.N - jc);  // columns of this chunk inside the matrix
+      const bool row_ok =
+          mrow < s.M && (ncols <= 0 || SWIGLU_CHECK_PTR(s.dbg, src, 2 * (int64_t)ncols, s.err));
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        w[q] = (mrow < s.M && jc + q * 8 + 8 <= s.N) ? src[q] : make_uint4(0, 0, 0, 0);
+        w[q] = (row_ok && jc + q * 8 + 8 <= s.N) ? src[q] : make_uint4(0, 0, 0, 0);
     };
     if constexpr (DIRECT) {
       load_row(wg, p.g, jt + c0 * 32);
@@ -410,8 +439,8 @@ struct EpiDSwiGLUT {
     } else {
       const int jc = jt + c0 * 32;
       auto ok = [&](int q) { return jc + q * 8 + 8 <= s.N; };
-      warp_load_issue(wg, lane, rows_of(p.g, jc), ok);
-      warp_load_issue(wu, lane, rows_of(p.u, jc), ok);
+      warp_load_issue(wg, lane, checked_rows(s, rows_of(p.g, jc), ok), ok);
+      warp_load_issue(wu, lane, checked_rows(s, rows_of(p.u, jc), ok), ok);
     }
 #pragma unroll 1
     for (int c = c0; c < c0 + CH; ++c) {
@@ -432,8 +461,8 @@ struct EpiDSwiGLUT {
         if (c + 1 < c0 + CH) {
           const int jn = jt + (c + 1) * 32;
           auto okn = [&](int q) { return jn + q * 8 + 8 <= s.N; };
-          warp_load_issue(wg, lane, rows_of(p.g, jn), okn);
-          warp_load_issue(wu, lane, rows_of(p.u, jn), okn);
+          warp_load_issue(wg, lane, checked_rows(s, rows_of(p.g, jn), okn), okn);
+          warp_load_issue(wu, lane, checked_rows(s, rows_of(p.u, jn), okn), okn);
         }
       }
       uint32_t r[32];
@@ -460,8 +489,8 @@ struct EpiDSwiGLUT {
       }
       const int jc = jt + c * 32;
       auto ok = [&](int q) { return jc + q * 8 + 8 <= s.N; };
-      warp_store_tile(buf, odg, lane, rows_of(p.g, jc), ok);
-      warp_store_tile(buf, odu, lane, rows_of(p.u, jc), ok);
+      warp_store_tile(buf, odg, lane, checked_rows(s, rows_of(p.g, jc), ok), ok);
+      warp_store_tile(buf, odu, lane, checked_rows(s, rows_of(p.u, jc), ok), ok);
     }
   }
 };
@@ -695,6 +724,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // of a warp write consecutive 16-byte groups)
         float4* slot = reinterpret_cast<float4*>(
             s.part + ((size_t)blockIdx.x * s.seg_max + seg) * (size_t)(TC_BM * BN));
+        const bool slot_ok = SWIGLU_CHECK(seg < s.seg_max, s.err) &&
+                             SWIGLU_CHECK_PTR(s.dbg, slot, (int64_t)TC_BM * BN * 4, s.err);
 #pragma unroll 1
         for (int c = half * CH; c < (half + 1) * CH; ++c) {
           uint32_t r[32];
@@ -702,9 +733,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int g = 0; g < 8; ++g)
-            slot[((c * 4 + quarter) * 8 + g) * 32 + lane] =
-                make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                            __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+            if (slot_ok)
+              slot[((c * 4 + quarter) * 8 + g) * 32 + lane] =
+                  make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                              __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
         }
         __threadfence();
         ++seg;
@@ -713,7 +745,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_epi_bar();
         if (e == 0) {
           int last = 0;
-          if (!*abort_flag) last = atomicAdd(s.counters + tile, 1) == c_last - c_first;
+          if (!*abort_flag)
+            last = SWIGLU_CHECK(tile < s.sk_tiles, s.err) &&
+                   atomicAdd(s.counters + tile, 1) == c_last - c_first;
           *last_flag = last;
         }
         tc_epi_bar();
@@ -739,9 +773,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int j = tile - (int)(sk_start(pc, sk_total, ctas) / s.k_blocks);
                 const float4* ps = reinterpret_cast<const float4*>(
                     s.part + ((size_t)pc * s.seg_max + j) * (size_t)(TC_BM * BN));
+                const bool ps_ok =
+                    SWIGLU_CHECK(j >= 0 && j < s.seg_max, s.err) &&
+                    SWIGLU_CHECK_PTR(s.dbg, ps, (int64_t)TC_BM * BN * 4, s.err);
                 float4 v[8];
 #pragma unroll
-                for (int g = 0; g < 8; ++g) v[g] = __ldcg(ps + ((c * 4 + quarter) * 8 + g) * 32 + lane);
+                for (int g = 0; g < 8; ++g)
+                  v[g] = ps_ok ? __ldcg(ps + ((c * 4 + quarter) * 8 + g) * 32 + lane)
+                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
                   sum[4 * g] += v[g].x;
@@ -757,7 +796,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tmem_st_32x32b_x32(tacc + c * 32, w);
           }
           tmem_st_wait();
-          if (e == 0) s.counters[tile] = 0;  // ready for the next launch
+          // ready for the next launch
+          if (e == 0 && SWIGLU_CHECK(tile < s.sk_tiles, s.err)) s.counters[tile] = 0;
           // the epilogue may read columns that another thread summed
           tc_fence_before();
           tc_epi_bar();

@@ -84,7 +84,8 @@ typedef enum {
   SWIGLU_ERR_UNSUPPORTED = 3,     /* shape outside the supported range (e.g. > 2^31 - 1 rows) */
   SWIGLU_ERR_WORKSPACE = 4,       /* ws is NULL or smaller than swiglu_mlp_workspace_bytes() */
   SWIGLU_ERR_CUDA = 5,            /* a CUDA runtime/driver call or a launch failed */
-  SWIGLU_ERR_DEVICE_TIMEOUT = 6   /* a device pipeline wait ran past its limit */
+  SWIGLU_ERR_DEVICE_TIMEOUT = 6,  /* a device pipeline wait ran past its limit */
+  SWIGLU_ERR_DEVICE_BOUNDS = 7    /* debug builds only: a device index check failed */
 } swiglu_status;
 
 /* Operations, for sizing queries. */
@@ -249,9 +250,30 @@ swiglu_status swiglu_mlp_bwd_ex(const void* dY, const void* X, const void* Wgu, 
                                 void* stream);
 
 /* Synchronises ``stream`` and reads the device error word in ``ws``:
- * SWIGLU_OK, SWIGLU_ERR_DEVICE_TIMEOUT, or SWIGLU_ERR_CUDA if the stream
- * reported an error. */
+ * SWIGLU_OK, SWIGLU_ERR_DEVICE_TIMEOUT, SWIGLU_ERR_DEVICE_BOUNDS (debug
+ * builds), or SWIGLU_ERR_CUDA if the stream reported an error. */
 swiglu_status swiglu_mlp_query_error(const void* ws, void* stream);
+
+/* 1 if this library was compiled as the debug build (-DSWIGLU_DEBUG, shipped
+ * as libswiglu_mlp_debug.so), else 0.  In the debug build every plain
+ * (non-TMA) global load and store of every kernel -- epilogue outputs, the
+ * dG/dU epilogue's reads of G and U, stream-K partial tiles, tile counters,
+ * the few-token queue and ready mask, the fp32 path's operands -- is checked
+ * against the buffers that launch was given (the caller's tensors and the
+ * workspace, with their sizes) and its table indices against their bounds.
+ * A failed check skips the access and records SWIGLU_ERR_DEVICE_BOUNDS in the
+ * workspace error word (read by swiglu_mlp_query_error); the kernel runs to
+ * its end, nothing traps.  Same API, same results; slower. */
+int swiglu_mlp_debug_build(void);
+
+/* Test hook for the debug build's checks: when ``on`` is nonzero, the next
+ * launch of this process gets its output buffer's window halved, so the
+ * kernel's accesses to the buffer's second half fail their check, are
+ * skipped, and SWIGLU_ERR_DEVICE_BOUNDS is recorded.  No access leaves the
+ * caller's buffers.  The flag clears itself after one launch.  Outputs of
+ * that call are undefined; the workspace stays valid.  In the release build
+ * the flag has no effect. */
+void swiglu_mlp_debug_narrow_once(int on);
 
 /* Static description of a status code. */
 const char* swiglu_status_string(swiglu_status status);

@@ -28,6 +28,21 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, n), n
 
 
+def test_debug_library_exports_the_same_symbols_and_says_what_it_is(L):
+    # libswiglu_mlp_debug.so: the same sources with the device index checks
+    D = api._load(api.DEBUG_LIB_PATH)
+    for n in api.declared_symbols():
+        assert hasattr(D, n), n
+    assert D.swiglu_mlp_debug_build() == 1 and L.swiglu_mlp_debug_build() == 0
+    assert D.swiglu_status_string(7) == b"device index check failed (debug build)"
+    assert api.STATUS[7] == "SWIGLU_ERR_DEVICE_BOUNDS"
+    # argument checks are the release build's
+    for args in [(None, None, None, None, None, 4, 64, 64, 0, None, 0, None),
+                 (None, None, None, None, None, -1, 64, 64, 0, None, 0, None),
+                 (None, None, None, None, None, 4, 60, 64, 0, None, 0, None)]:
+        assert D.swiglu_mlp_fwd(*args) == L.swiglu_mlp_fwd(*args) != OK
+
+
 def test_sizes(L):
     assert L.swiglu_mlp_element_bytes(0) == 2
     assert L.swiglu_mlp_element_bytes(1) == 2
