@@ -182,9 +182,11 @@ int sm_count() {
 }
 
 // 2-D tiled map over a row-major matrix [outer][inner] (inner contiguous) with
-// a row stride in bytes; 128-byte swizzle; out-of-range elements read as 0.
+// a row stride in bytes; 128-byte swizzle unless given; out-of-range elements
+// read as 0 (and are not written by a store).
 bool encode_2d(CUtensorMap* tm, bool bf16, const void* base, uint64_t inner, uint64_t outer,
-               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -193,7 +195,7 @@ bool encode_2d(CUtensorMap* tm, bool bf16, const void* base, uint64_t inner, uin
   cuuint32_t estr[2] = {1, 1};
   return enc(tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -417,11 +419,16 @@ cudaError_t launch_tc(int kid, const CUtensorMap& ta, const CUtensorMap& tb, con
 }
 
 // The pair kernel: clusters of two CTAs on the two SMs of a TPC.
+// tg, tu: the TMA dG/dU epilogue's maps of G and U (other epilogues: unused)
 template <int AM, int BMODE, bool BF16, class Epi>
 cudaError_t launch_tc2(int kid, const CUtensorMap& ta, const CUtensorMap& tb, const TcShape& s,
-                       const typename Epi::Params& ep, cudaStream_t st) {
-  auto kern = tc2_gemm_kernel<TC2_STAGES, AM, BMODE, BF16, Epi>;
-  constexpr int smem = Tc2Smem<TC2_STAGES>::DYN_BYTES;
+                       const typename Epi::Params& ep, cudaStream_t st,
+                       const CUtensorMap* tg = nullptr, const CUtensorMap* tu = nullptr) {
+  // the TMA dG/dU epilogue's slots take the room of two ring stages
+  constexpr bool gu = epi_tma_gu<Epi>::value;
+  constexpr int stages = gu ? TC2_STAGES - 2 : TC2_STAGES;
+  auto kern = tc2_gemm_kernel<stages, AM, BMODE, BF16, Epi>;
+  constexpr int smem = Tc2Smem<stages, gu>::DYN_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int units = launch_units(s, tc2_units());
@@ -438,7 +445,8 @@ cudaError_t launch_tc2(int kid, const CUtensorMap& ta, const CUtensorMap& tb, co
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   ProfScope prof(kid, st);
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, s, ep);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, s, ep, tg != nullptr ? *tg : ta,
+                         tu != nullptr ? *tu : tb);
   g_last_launches.fetch_add(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -893,11 +901,22 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     TcShape s = make_shape(M, H, D, TC_BN, err, pairs, cap);
     set_windows(s, {{saved, (size_t)(M * ld * 2)}, {err, ws_bytes}});
     EpiDSwiGLU::Params p{G, U, ld, o.gm, o.dm};
-    // a short contraction leaves the epilogue the bound: direct G/U loads
-    e = D <= 2048 ? launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLUT<true>>(
-                        pairs, K_DGU, m1, m2, s, p, st)
-                  : launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLUT<false>>(
-                        pairs, K_DGU, m1, m2, s, p, st);
+    if (pairs && D <= 2048) {
+      // a short contraction leaves the epilogue the bound: G/U in and dG/dU
+      // out by TMA, through per-warp slots loaded ahead
+      CUtensorMap tg, tu;
+      if (!encode_2d(&tg, BF16, G, H, M, ld * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+          !encode_2d(&tu, BF16, U, H, M, ld * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return SWIGLU_ERR_CUDA;
+      e = launch_tc2<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLUTma>(
+          K_DGU, m1, m2, s, EpiDSwiGLUTma::Params{o.gm, o.dm}, st, &tg, &tu);
+    } else {
+      // a short contraction on single SMs: direct G/U loads
+      e = D <= 2048 ? launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLUT<true>>(
+                          pairs, K_DGU, m1, m2, s, p, st)
+                    : launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiDSwiGLUT<false>>(
+                          pairs, K_DGU, m1, m2, s, p, st);
+    }
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   // [dWg; dWu] [2H, D] = [dG | dU]^T X: one GEMM over the 2H columns

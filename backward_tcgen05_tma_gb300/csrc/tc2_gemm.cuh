@@ -29,27 +29,168 @@ namespace swiglu {
 constexpr int TC2_BM = 256;  // output rows per tile (128 per CTA)
 constexpr int TC2_BN = 256;
 
-template <int STAGES>
+// The TMA form of the dG/dU epilogue: each epilogue warp streams its 32 x 32
+// chunks of G and U through GU_SLOTS shared-memory slots (G box, then U box).
+constexpr int GU_SLOTS = 3;
+constexpr int GU_SLOT_BYTES = 4096;
+constexpr int GU_CHUNKS = TC2_BN / 64;  // 32-column chunks per warp and tile
+
+// GU: the epilogue is the TMA dG/dU form (G/U slots and their barriers
+// instead of the 2 KB store-staging buffers).
+template <int STAGES, bool GU = false>
 struct Tc2Smem {
   static constexpr int A_BYTES = 128 * TC_BK * 2;  // this CTA's 128 rows of A
   static constexpr int B_BYTES = 128 * TC_BK * 2;  // this CTA's 128 columns of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;  // 8 warps x 2 KB store staging
-  static constexpr int BAR_OFFSET = EPI_OFFSET + 8 * 2048;
-  // barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int GU_OFFSET = EPI_OFFSET + (GU ? 0 : 8 * 2048);  // 8 warps x GU_SLOTS slots
+  static constexpr int BAR_OFFSET = GU_OFFSET + (GU ? 8 * GU_SLOTS * GU_SLOT_BYTES : 0);
+  // barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain,
+  // then (GU) one per G/U slot
+  static constexpr int GU_BAR = 2 * STAGES + 5;
+  static constexpr int NUM_BARS = GU_BAR + (GU ? 8 * GU_SLOTS : 0);
   static constexpr int MISC_OFFSET = BAR_OFFSET + NUM_BARS * 8;  // tmem slot, abort, last
   static constexpr int TOTAL = MISC_OFFSET + 16;
   static constexpr int DYN_BYTES = TOTAL + 1024;
   static constexpr int TMEM_COLS = 2 * TC2_BN;
 };
 
+// Backward SwiGLU epilogue (the math of EpiDSwiGLUT) with its G/U traffic on
+// TMA: per warp, G and U arrive in 32 x 32 boxes (64-byte swizzle, so that
+// each lane reads its row without bank conflicts) up to two chunks ahead --
+// across tiles too, when the next tile is taken whole -- and dG, dU are
+// written back into the same slot and leave by TMA store.  The tensor maps
+// bound both directions at M rows and H columns (ragged tiles need no
+// checks), and no register holds a prefetched chunk.  With a short
+// contraction (K = D <= 2048) the epilogue bounds this GEMM and its loads,
+// issued one chunk ahead from registers, were latency-bound.
+struct EpiDSwiGLUTma {
+  static constexpr bool TMA_GU = true;
+  // the kernel's tensor maps tmG (G [M][H] within the saved rows, row stride
+  // 3H, box 32 x 32) and tmU (U, the same at column offset H) carry G and U
+  struct Params {
+    float gate_mul, down_mul;
+  };
+};
+
+template <class E, class = void>
+struct epi_tma_gu {
+  static constexpr bool value = false;
+};
+template <class E>
+struct epi_tma_gu<E, decltype((void)E::TMA_GU)> {
+  static constexpr bool value = E::TMA_GU;
+};
+
+// One epilogue warp's stream of G/U jobs: job k (one 32 x 32 chunk) uses
+// slot k % GU_SLOTS and that slot's barrier phase (k / GU_SLOTS) & 1.  The
+// issue cursor walks the chunks of a tile (row0, col0), then of the next
+// tile if it is known to run its epilogue.
+struct GuPipe {
+  uint32_t slot0, bar0;      // slot 0's shared address and barrier
+  uint32_t issued, done;     // jobs whose loads were issued / whose stores were issued
+  int cur_row0, cur_col0, cur_c;  // next job to issue: chunk cur_c (GU_CHUNKS: none)
+  int nxt_row0, nxt_col0;
+  bool nxt;
+
+  // Issue jobs up to index kmax (lane 0 issues; every lane keeps the count).
+  __device__ __forceinline__ void issue_upto(uint32_t kmax, const CUtensorMap* gm,
+                                             const CUtensorMap* um, int lane) {
+    while (issued <= kmax && cur_c < GU_CHUNKS) {
+      const uint32_t b = issued % GU_SLOTS;
+      if (lane == 0) {
+        // the slot's previous job stored from it one chunk or more ago
+        bulk_wait_group_read<0>();
+        const uint32_t bar = bar0 + 8u * b, dst = slot0 + GU_SLOT_BYTES * b;
+        mbar_arrive_expect_tx(bar, GU_SLOT_BYTES);
+        tma_load_2d(dst, gm, bar, cur_col0 + cur_c * 32, cur_row0);
+        tma_load_2d(dst + 2048, um, bar, cur_col0 + cur_c * 32, cur_row0);
+      }
+      ++issued;
+      if (++cur_c == GU_CHUNKS && nxt) {
+        cur_row0 = nxt_row0;
+        cur_col0 = nxt_col0;
+        cur_c = 0;
+        nxt = false;
+      }
+    }
+  }
+};
+
+// One tile's dG/dU for this warp's 32 rows (from row0) and GU_CHUNKS chunks
+// (from column col0; TMEM columns from tacc) of the M x H matrices.  nxt:
+// the next tile of this CTA, if taken whole (its epilogue certainly runs),
+// whose first chunks may be loaded during this one.  Loads of boxes outside
+// the matrices read zeros; stores of boxes wholly outside are not issued.
+// Returns false if a wait ran out.
+template <bool BF16>
+__device__ __forceinline__ bool dgu_tma_tile(GuPipe& gp, const CUtensorMap* gm,
+                                             const CUtensorMap* um, const EpiDSwiGLUTma::Params& p,
+                                             uint32_t tacc, int row0, int col0, int M, int H,
+                                             bool nxt, int nrow0, int ncol0, int lane,
+                                             uint8_t* slots, uint64_t wl, volatile int* abort_flag,
+                                             int* err) {
+  if (gp.cur_c == GU_CHUNKS) {  // nothing of this tile issued ahead
+    gp.cur_row0 = row0;
+    gp.cur_col0 = col0;
+    gp.cur_c = 0;
+  }
+  gp.nxt = nxt;
+  gp.nxt_row0 = nrow0;
+  gp.nxt_col0 = ncol0;
+  const int sw = (lane >> 1) & 3;  // 64-byte swizzle: 16-byte unit q of row r at q ^ ((r / 2) % 4)
+#pragma unroll 1
+  for (int c = 0; c < GU_CHUNKS; ++c) {
+    const uint32_t k = gp.done;
+    gp.issue_upto(k + 1, gm, um, lane);
+    const uint32_t b = k % GU_SLOTS;
+    const int ok = mbar_wait_bounded(gp.bar0 + 8u * b, (k / GU_SLOTS) & 1u, wl, abort_flag, err);
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    uint8_t* gs = slots + GU_SLOT_BYTES * b + lane * 64;
+    uint8_t* us = gs + 2048;
+    uint4 vg[4], vu[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      vg[q] = *reinterpret_cast<const uint4*>(gs + ((q ^ sw) << 4));
+      vu[q] = *reinterpret_cast<const uint4*>(us + ((q ^ sw) << 4));
+    }
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tacc + c * 32, r);
+    tmem_ld_wait();
+    uint32_t odg[16], odu[16];
+    dswiglu_32<BF16>(vg, vu, r, p.gate_mul, p.down_mul, odg, odu);
+    // two chunks ahead, into the slot whose stores left one chunk ago
+    gp.issue_upto(k + 2, gm, um, lane);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      *reinterpret_cast<uint4*>(gs + ((q ^ sw) << 4)) =
+          make_uint4(odg[4 * q], odg[4 * q + 1], odg[4 * q + 2], odg[4 * q + 3]);
+      *reinterpret_cast<uint4*>(us + ((q ^ sw) << 4)) =
+          make_uint4(odu[4 * q], odu[4 * q + 1], odu[4 * q + 2], odu[4 * q + 3]);
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t src = gp.slot0 + GU_SLOT_BYTES * b;
+      if (row0 < M && col0 + c * 32 < H) {
+        tma_store_2d(gm, src, col0 + c * 32, row0);
+        tma_store_2d(um, src + 2048, col0 + c * 32, row0);
+      }
+      bulk_commit_group();  // (an empty group when nothing was stored)
+    }
+    ++gp.done;
+  }
+  return true;
+}
+
 template <int STAGES, int A_MODE, int B_MODE, bool BF16, class Epi>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const TcShape s,
-                    const typename Epi::Params ep) {
-  using L = Tc2Smem<STAGES>;
+                    const typename Epi::Params ep, const __grid_constant__ CUtensorMap tmG,
+                    const __grid_constant__ CUtensorMap tmU) {
+  constexpr bool TMA_GU = epi_tma_gu<Epi>::value;
+  using L = Tc2Smem<STAGES, TMA_GU>;
   constexpr int BN = TC2_BN;
   static_assert(L::TOTAL + 1024 <= 232448, "shared memory plan exceeds 227 KB");
 
@@ -82,6 +223,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(acce_bar(i), 16);  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(drain_bar, 1);
+    if constexpr (TMA_GU)
+      for (int i = 0; i < 8 * GU_SLOTS; ++i) mbar_init(bar0 + 8u * (L::GU_BAR + i), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -233,6 +376,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int seg = 0;  // shared segments done (= partial slot index)
+    GuPipe gp;    // TMA dG/dU epilogue: this warp's G/U job stream
+    gp.slot0 = sbase + L::GU_OFFSET + (warp - 2) * GU_SLOTS * GU_SLOT_BYTES;
+    gp.bar0 = bar0 + 8u * (L::GU_BAR + (warp - 2) * GU_SLOTS);
+    gp.issued = gp.done = 0;
+    gp.cur_c = GU_CHUNKS;
+    gp.nxt = false;
+    int gu_ok = 1;
     TcSegIter it = segs();
     int tile, kb0, nkb;
     bool whole;
@@ -241,7 +391,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (lane == 0)
         ok = mbar_wait_bounded(accf_bar(acc), acc_phase, s.wait_limit_ns, abort_flag, s.err) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!tc_epi_bar_and(ok)) break;
+      if (!tc_epi_bar_and(ok && gu_ok)) break;
       tc_fence_after();
       int mt, nt;
       tc_tile_coords(tile, s, mt, nt);
@@ -330,9 +480,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tc_fence_after();
         }
       }
-      if (run_epi)
-        Epi::template run<BN, BF16>(ep, s, tacc, mt * TC2_BM + (int)rank * 128, nt, row, half,
-                                    smem + L::EPI_OFFSET + (warp - 2) * 2048);
+      if (run_epi) {
+        if constexpr (TMA_GU) {
+          // the next segment, when whole, certainly runs its epilogue next
+          TcSegIter pk = it;
+          int t2, kb2, nkb2, mt2 = 0, nt2 = 0;
+          bool w2 = false;
+          const bool nx = pk.next(t2, kb2, nkb2, w2) && w2;
+          if (nx) tc_tile_coords(t2, s, mt2, nt2);
+          const int rq = (int)rank * 128 + quarter * 32;
+          gu_ok = dgu_tma_tile<BF16>(gp, &tmG, &tmU, ep, tacc + half * CH * 32, mt * TC2_BM + rq,
+                                     nt * BN + half * (BN / 2), s.M, s.N, nx, mt2 * TC2_BM + rq,
+                                     nt2 * BN + half * (BN / 2), lane,
+                                     smem + L::GU_OFFSET + (warp - 2) * GU_SLOTS * GU_SLOT_BYTES,
+                                     s.wait_limit_ns, abort_flag, s.err)
+                      ? 1
+                      : 0;
+        } else {
+          Epi::template run<BN, BF16>(ep, s, tacc, mt * TC2_BM + (int)rank * 128, nt, row, half,
+                                      smem + L::EPI_OFFSET + (warp - 2) * 2048);
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
@@ -340,6 +508,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         acc = 0;
         acc_phase ^= 1u;
       }
+    }
+    if constexpr (TMA_GU) {
+      if (lane == 0) {
+        // loads issued ahead but never used (the loop ended early) land
+        // before the CTA exits; the dG/dU stores complete
+        for (uint32_t k = gp.done; k < gp.issued; ++k)
+          mbar_wait_bounded(gp.bar0 + 8u * (k % GU_SLOTS), (k / GU_SLOTS) & 1u, s.wait_limit_ns,
+                            nullptr, s.err);
+        bulk_wait_group<0>();
+      }
+      __syncwarp();
     }
   }
 

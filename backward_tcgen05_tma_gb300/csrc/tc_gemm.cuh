@@ -392,6 +392,35 @@ struct EpiSwiGLU {
 // and its shared-memory traffic.  With a short contraction (K = D <= 2048)
 // the epilogue bounds this GEMM and the direct form is 13% faster; with a
 // long one the tensor core does and the staged form is 3% faster.
+// dU = rnd(dA SiLU(g)), dG = rnd(dA u SiLU'(g) gate_mul) for 32 columns of
+// one row: g, u packed in vg, vu (8 words of 2 each); r = the accumulator's
+// 32 fp32 columns (dA = down_mul r).
+template <bool BF16>
+__device__ __forceinline__ void dswiglu_32(const uint4 (&vg)[4], const uint4 (&vu)[4],
+                                           const uint32_t (&r)[32], float gate_mul,
+                                           float down_mul, uint32_t (&odg)[16],
+                                           uint32_t (&odu)[16]) {
+  using P = Pack<BF16>;
+#pragma unroll
+  for (int g8 = 0; g8 < 4; ++g8) {
+    const uint32_t* pg = &vg[g8].x;
+    const uint32_t* pu = &vu[g8].x;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 g = P::unpack(pg[e]);
+      const float2 u = P::unpack(pu[e]);
+      const float da0 = down_mul * __uint_as_float(r[g8 * 8 + 2 * e]);
+      const float da1 = down_mul * __uint_as_float(r[g8 * 8 + 2 * e + 1]);
+      const float s0 = sigmoid_f32(g.x);
+      const float s1 = sigmoid_f32(g.y);
+      const float ds0 = s0 * (1.0f + g.x * (1.0f - s0)) * gate_mul;
+      const float ds1 = s1 * (1.0f + g.y * (1.0f - s1)) * gate_mul;
+      odu[g8 * 4 + e] = P::two(da0 * (g.x * s0), da1 * (g.y * s1));
+      odg[g8 * 4 + e] = P::two(da0 * u.x * ds0, da1 * u.y * ds1);
+    }
+  }
+}
+
 struct EpiDSwiGLUParams {
   void* g;  // G (becomes dG); U (becomes dU) at u
   void* u;
@@ -469,24 +498,7 @@ struct EpiDSwiGLUT {
       tmem_ld_32x32b_x32(tacc + c * 32, r);
       tmem_ld_wait();
       uint32_t odg[16], odu[16];
-#pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        const uint32_t* pg = &vg[g8].x;
-        const uint32_t* pu = &vu[g8].x;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 g = P::unpack(pg[e]);
-          const float2 u = P::unpack(pu[e]);
-          const float da0 = p.down_mul * __uint_as_float(r[g8 * 8 + 2 * e]);
-          const float da1 = p.down_mul * __uint_as_float(r[g8 * 8 + 2 * e + 1]);
-          const float s0 = sigmoid_f32(g.x);
-          const float s1 = sigmoid_f32(g.y);
-          const float ds0 = s0 * (1.0f + g.x * (1.0f - s0)) * p.gate_mul;
-          const float ds1 = s1 * (1.0f + g.y * (1.0f - s1)) * p.gate_mul;
-          odu[g8 * 4 + e] = P::two(da0 * (g.x * s0), da1 * (g.y * s1));
-          odg[g8 * 4 + e] = P::two(da0 * u.x * ds0, da1 * u.y * ds1);
-        }
-      }
+      dswiglu_32<BF16>(vg, vu, r, p.gate_mul, p.down_mul, odg, odu);
       const int jc = jt + c * 32;
       auto ok = [&](int q) { return jc + q * 8 + 8 <= s.N; };
       warp_store_tile(buf, odg, lane, checked_rows(s, rows_of(p.g, jc), ok), ok);
