@@ -424,9 +424,9 @@ template <int AM, int BMODE, bool BF16, class Epi>
 cudaError_t launch_tc2(int kid, const CUtensorMap& ta, const CUtensorMap& tb, const TcShape& s,
                        const typename Epi::Params& ep, cudaStream_t st,
                        const CUtensorMap* tg = nullptr, const CUtensorMap* tu = nullptr) {
-  // the TMA dG/dU epilogue's slots take the room of two ring stages
+  // the TMA dG/dU epilogue's slots take the room of one ring stage
   constexpr bool gu = epi_tma_gu<Epi>::value;
-  constexpr int stages = gu ? TC2_STAGES - 2 : TC2_STAGES;
+  constexpr int stages = gu ? TC2_STAGES - 1 : TC2_STAGES;
   auto kern = tc2_gemm_kernel<stages, AM, BMODE, BF16, Epi>;
   constexpr int smem = Tc2Smem<stages, gu>::DYN_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
