@@ -349,8 +349,10 @@ def swiglu_mlp_set_wait_limit_ns(ns: int) -> int:
     return int(lib().swiglu_mlp_set_wait_limit_ns(int(ns)))
 
 
-def swiglu_mlp_inject_stall_once(on: bool = True) -> None:
-    lib().swiglu_mlp_inject_stall_once(1 if on else 0)
+def swiglu_mlp_inject_stall_once(on: bool | int = True) -> None:
+    """True / 1: stall the next tensor-core launch; n: the n-th from now;
+    False / 0: clear."""
+    lib().swiglu_mlp_inject_stall_once(int(on))
 
 
 def swiglu_mlp_last_launch_count() -> int:

@@ -93,7 +93,16 @@ struct Opts {
   float gm = 1.0f, dm = 1.0f;
   int acc = 0;
 };
-std::atomic<int> g_inject_stall{0};
+std::atomic<int> g_inject_stall{0};  // launches until the injected stall (0: none)
+
+// The stall-injection countdown (swiglu_mlp_inject_stall_once): true for the
+// one launch it reaches.
+bool take_inject() {
+  int v = g_inject_stall.load();
+  while (v > 0 && !g_inject_stall.compare_exchange_weak(v, v - 1)) {
+  }
+  return v == 1;
+}
 std::atomic<int> g_last_launches{0};
 std::atomic<int> g_cta_pairs{1};  // SM pairs (cta_group::2): 0 never, 1 by size, 2 always
 std::atomic<int> g_ng_fused{1};   // few-token no-grad: fused kernel 0 never, 1 by size, 2 always
@@ -377,7 +386,7 @@ TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err
   s.group_m = 16;
   s.wait_limit_ns = g_wait_limit_ns.load();
   s.err = err;
-  s.inject_stall = g_inject_stall.exchange(0);
+  s.inject_stall = take_inject() ? 1 : 0;
   // the workspace (whose first word is err) carries the stream-K scratch
   const TcPlan p = tc_plan((int64_t)s.m_tiles * s.n_tiles, s.k_blocks,
                            pairs ? tc2_units() : tc_nsm());
@@ -694,7 +703,7 @@ swiglu_status ng_forward_fused(const void* X, const void* Wgu, const void* Wd, v
   f.ready = reinterpret_cast<uint32_t*>(counters + p.t1 + p.t2);
   f.next_unit = reinterpret_cast<uint32_t*>(ws + NG_NEXT_OFFSET);
   f.done = reinterpret_cast<uint32_t*>(ws + NG_DONE_OFFSET);
-  f.inject_unready = g_inject_stall.exchange(0);
+  f.inject_unready = take_inject() ? 1 : 0;
   float* part0 = reinterpret_cast<float*>(ws + WS_HEADER + p.counter_bytes);
   float* part1 = reinterpret_cast<float*>(ws + WS_HEADER + p.counter_bytes + d.part0_bytes);
   const uint64_t wl = g_wait_limit_ns.load();
@@ -1290,7 +1299,7 @@ uint64_t swiglu_mlp_set_wait_limit_ns(uint64_t ns) {
   return g_wait_limit_ns.exchange(ns);
 }
 
-void swiglu_mlp_inject_stall_once(int on) { g_inject_stall.store(on ? 1 : 0); }
+void swiglu_mlp_inject_stall_once(int on) { g_inject_stall.store(on > 0 ? on : 0); }
 
 int swiglu_mlp_last_launch_count(void) { return g_last_launches.load(); }
 

@@ -283,12 +283,14 @@ const char* swiglu_status_string(swiglu_status status);
  * 1000).  Returns the previous limit. */
 uint64_t swiglu_mlp_set_wait_limit_ns(uint64_t ns);
 
-/* Test hook for failure detection: when ``on`` is nonzero, the next
- * tensor-core launch of this process makes its load producer skip the arrival
- * of the first pipeline stage (or, in the fused few-token no-grad kernel,
- * leaves the first gate/up tile's ready bit clear), so a consumer's wait runs
- * out, the kernel records SWIGLU_ERR_DEVICE_TIMEOUT and returns cleanly.  The
- * flag clears itself after one launch.  Outputs of that call are undefined. */
+/* Test hook for failure detection: when ``on`` = n > 0, the n-th
+ * tensor-core launch of this process from now (1: the next) makes its load
+ * producer skip the arrival of the first pipeline stage (or, in the fused
+ * few-token no-grad kernel, leaves the first gate/up tile's ready bit clear),
+ * so a consumer's wait runs out, the kernel records SWIGLU_ERR_DEVICE_TIMEOUT
+ * and returns cleanly.  Training launches come in the order gate/up, down
+ * (forward) and dWd, dG/dU, dWgu, dX (backward).  The hook clears itself at
+ * that launch; on <= 0 clears it.  Outputs of that call are undefined. */
 void swiglu_mlp_inject_stall_once(int on);
 
 /* Selects how later calls of this process run their bf16/fp16 tensor-core

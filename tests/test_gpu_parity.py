@@ -231,6 +231,31 @@ def test_stalled_pipeline_times_out_cleanly(cta_pairs):
     check_all(g, run_oracle(t, "bf16"), "bf16")
 
 
+def test_stalled_tma_dgu_kernel_times_out_cleanly():
+    """The same failure, injected into the dG/dU kernel of a backward call (its
+    second launch) on SM pairs with D <= 2048, where the epilogue streams G/U
+    through TMA slots: the kernel unwinds, reports the timeout, and the next
+    backward on fresh buffers is correct."""
+    M, D, H = 512, 256, 512
+    t = synthetic.make_inputs(M, D, H, "bf16", seed=12, device="cuda")
+    old_p = api.swiglu_mlp_set_cta_pairs(2)
+    old = api.swiglu_mlp_set_wait_limit_ns(20_000_000)  # 20 ms
+    try:
+        _, saved = api.swiglu_mlp_fwd(t["X"], t["Wgu"], t["Wd"])
+        ws = api.workspace(M, D, H, torch.bfloat16, 2, "cuda")
+        api.swiglu_mlp_inject_stall_once(2)  # dWd, then dG/dU
+        api.swiglu_mlp_bwd(t["dY"], t["X"], t["Wgu"], t["Wd"], saved, ws=ws)
+        assert api.swiglu_mlp_query_error(ws) == 6
+    finally:
+        api.swiglu_mlp_inject_stall_once(False)
+        api.swiglu_mlp_set_wait_limit_ns(old)
+    try:
+        g = run_gpu(t, "bf16")
+    finally:
+        api.swiglu_mlp_set_cta_pairs(old_p)
+    check_all(g, run_oracle(t, "bf16"), "bf16")
+
+
 # --------------------------------------------------------------------------
 # full-size workloads: sampled rows and hidden units against the oracle
 # --------------------------------------------------------------------------
