@@ -471,12 +471,30 @@ def _cpu_baseline(t_dev, w):
          for k in ("X", "dY", "Wg", "Wu", "Wd")}
     t0 = time.perf_counter()
     f = oracle.forward(c["X"], c["Wg"], c["Wu"], c["Wd"])
-    oracle.backward(c["dY"], c["X"], c["Wg"], c["Wu"], c["Wd"], f)
+    b = oracle.backward(c["dY"], c["X"], c["Wg"], c["Wu"], c["Wd"], f)
     dt = time.perf_counter() - t0
     return {"value": metrics.fwd_bwd_flops(m, D, H) / dt / 1e12, "unit": "TFLOPS",
             "cores": oracle.num_threads(), "kind": "oracle",
             "sample": "fwd+bwd of %d token rows (full D=%d, H=%d weights) of the workload, "
-                      "fp64 loops, %.1f s" % (m, D, H, dt)}
+                      "fp64 loops, %.1f s" % (m, D, H, dt),
+            "parity": _sample_parity(t_dev, f, b)}
+
+
+def _sample_parity(t_dev, f, b):
+    """The same sample through the library (C ABI, the training kernels):
+    relative Frobenius error of each output against the oracle's."""
+    import numpy as np
+    import oracle
+    from backward_tcgen05_tma_gb300 import api
+    Y, saved = api.swiglu_mlp_fwd(t_dev["X"], t_dev["Wgu"], t_dev["Wd"])
+    dX, dWgu, dWd = api.swiglu_mlp_bwd(t_dev["dY"], t_dev["X"], t_dev["Wgu"], t_dev["Wd"], saved)
+    H = t_dev["Wd"].shape[1]
+    got = {"Y": Y, "dX": dX, "dWg": dWgu[:H], "dWu": dWgu[H:], "dWd": dWd}
+    ref = {"Y": f["Y"], "dX": b["dX"], "dWg": b["dWg"], "dWu": b["dWu"], "dWd": b["dWd"]}
+    out = {k: float("%.3e" % oracle.rel_frob(got[k].double().cpu().numpy(), np.asarray(ref[k])))
+           for k in got}
+    out["metric"] = "relative Frobenius error vs the oracle (tolerance 1e-2)"
+    return out
 
 
 def run_nograd_only(args):
