@@ -186,6 +186,16 @@ def _check(code: int, where: str):
         raise SwigluError(code, where)
 
 
+def _device_check(ws, where: str):
+    """While the debug build is in use: wait for the call and raise on the
+    device status in its workspace (a failed index check, a timeout).  The
+    release build returns at once, as every call is asynchronous."""
+    if _use_debug:
+        code = int(lib().swiglu_mlp_query_error(_ptr(ws), _stream(ws.device)))
+        if code != 0:
+            raise SwigluError(code, where + " (device)")
+
+
 def workspace(M: int, D: int, H: int, dtype: torch.dtype, op: int, device,
               minimal: bool = False) -> torch.Tensor:
     """A zero-filled workspace: the recommended size, or with ``minimal`` the
@@ -222,6 +232,7 @@ def swiglu_mlp_fwd(X, Wgu, Wd, out: dict | None = None, ws=None, gate_mul: float
                                    dtype_code(X.dtype), _opts(gate_mul, down_mul, False),
                                    _ptr(ws), ws.numel(), _stream(X.device)),
            "swiglu_mlp_fwd")
+    _device_check(ws, "swiglu_mlp_fwd")
     return Y, saved
 
 
@@ -240,6 +251,7 @@ def swiglu_mlp_fwd_nograd(X, Wgu, Wd, out: dict | None = None, ws=None, gate_mul
                                           _opts(gate_mul, down_mul, False), _ptr(ws), ws.numel(),
                                           _stream(X.device)),
            "swiglu_mlp_fwd_nograd")
+    _device_check(ws, "swiglu_mlp_fwd_nograd")
     return Y, A
 
 
@@ -292,6 +304,11 @@ class FwdNogradGraph:
         s = torch.cuda.current_stream(self.X.device) if stream is None else stream
         _check(self._L.swiglu_mlp_graph_launch(self._h, ctypes.c_void_p(s.cuda_stream)),
                "swiglu_mlp_graph_launch")
+        if _use_debug:  # as _device_check, with the graph's own library
+            code = int(self._L.swiglu_mlp_query_error(_ptr(self.ws),
+                                                      ctypes.c_void_p(s.cuda_stream)))
+            if code != 0:
+                raise SwigluError(code, "swiglu_mlp_graph_launch (device)")
 
     def __call__(self, x=None):
         if x is not None and x.data_ptr() != self.X.data_ptr():
@@ -337,6 +354,7 @@ def swiglu_mlp_bwd(dY, X, Wgu, Wd, saved, out: dict | None = None, ws=None,
                                    dtype_code(X.dtype), _opts(gate_mul, down_mul, accumulate),
                                    _ptr(ws), ws.numel(), _stream(X.device)),
            "swiglu_mlp_bwd")
+    _device_check(ws, "swiglu_mlp_bwd")
     return dX, dWgu, dWd
 
 

@@ -35,14 +35,12 @@ def _built():
     prev = api.use_debug_library(True)
     assert api.lib().swiglu_mlp_debug_build() == 1
     api.use_debug_library(prev)
-    yield
-    api.use_debug_library(False)
 
 
 def with_library(debug, fn, pairs=1, fused=1):
     """fn() under the release or the debug build, with the SM-pair and
     few-token modes set in that library for the call."""
-    api.use_debug_library(debug)
+    prev = api.use_debug_library(debug)
     old_p = api.swiglu_mlp_set_cta_pairs(pairs)
     old_f = api.swiglu_mlp_set_nograd_fused(fused)
     try:
@@ -50,7 +48,7 @@ def with_library(debug, fn, pairs=1, fused=1):
     finally:
         api.swiglu_mlp_set_cta_pairs(old_p)
         api.swiglu_mlp_set_nograd_fused(old_f)
-        api.use_debug_library(False)
+        api.use_debug_library(prev)
 
 
 def same_in_both(fn, **modes):
@@ -152,15 +150,17 @@ def test_debug_build_matches_the_oracle():
 def narrowed_status(debug, call):
     """Status of call() (which returns its workspace) with the next launch's
     output window halved by the test hook."""
-    api.use_debug_library(debug)
+    prev = api.use_debug_library(debug)
     try:
         api.lib().swiglu_mlp_debug_narrow_once(1)
-        ws = call()
-        st = api.swiglu_mlp_query_error(ws)
+        try:
+            st = api.swiglu_mlp_query_error(call())
+        except api.SwigluError as e:  # with the debug build the binding checks each call
+            st = e.code
         api.lib().swiglu_mlp_debug_narrow_once(0)
         return st
     finally:
-        api.use_debug_library(False)
+        api.use_debug_library(prev)
 
 
 @pytest.mark.parametrize("path", ["training", "fused_nograd", "two_kernel_nograd", "fp32"])
@@ -175,9 +175,11 @@ def test_a_narrowed_window_is_reported_not_accessed(path):
             api.swiglu_mlp_fwd(t["X"], t["Wgu"], t["Wd"], ws=ws)
         else:
             old = api.swiglu_mlp_set_nograd_fused(2 if path == "fused_nograd" else 0)
-            ws = api.workspace(M, D, H, t["X"].dtype, api.SWIGLU_OP_FWD_NOGRAD, t["X"].device)
-            api.swiglu_mlp_fwd_nograd(t["X"], t["Wgu"], t["Wd"], ws=ws)
-            api.swiglu_mlp_set_nograd_fused(old)
+            try:
+                ws = api.workspace(M, D, H, t["X"].dtype, api.SWIGLU_OP_FWD_NOGRAD, t["X"].device)
+                api.swiglu_mlp_fwd_nograd(t["X"], t["Wgu"], t["Wd"], ws=ws)
+            finally:
+                api.swiglu_mlp_set_nograd_fused(old)
         return ws
 
     assert narrowed_status(True, call) == BOUNDS

@@ -9,6 +9,7 @@ import torch
 
 import oracle
 from backward_tcgen05_tma_gb300 import api, build, synthetic
+from tests.conftest import device_status
 
 pytestmark = pytest.mark.gpu
 
@@ -219,8 +220,7 @@ def test_stalled_pipeline_times_out_cleanly(cta_pairs):
     old = api.swiglu_mlp_set_wait_limit_ns(20_000_000)  # 20 ms
     try:
         api.swiglu_mlp_inject_stall_once(True)
-        api.swiglu_mlp_fwd(t["X"], t["Wgu"], t["Wd"], ws=ws)
-        assert api.swiglu_mlp_query_error(ws) == 6
+        assert device_status(lambda: api.swiglu_mlp_fwd(t["X"], t["Wgu"], t["Wd"], ws=ws), ws) == 6
     finally:
         api.swiglu_mlp_inject_stall_once(False)
         api.swiglu_mlp_set_wait_limit_ns(old)
@@ -244,8 +244,8 @@ def test_stalled_tma_dgu_kernel_times_out_cleanly():
         _, saved = api.swiglu_mlp_fwd(t["X"], t["Wgu"], t["Wd"])
         ws = api.workspace(M, D, H, torch.bfloat16, 2, "cuda")
         api.swiglu_mlp_inject_stall_once(2)  # dWd, then dG/dU
-        api.swiglu_mlp_bwd(t["dY"], t["X"], t["Wgu"], t["Wd"], saved, ws=ws)
-        assert api.swiglu_mlp_query_error(ws) == 6
+        assert device_status(
+            lambda: api.swiglu_mlp_bwd(t["dY"], t["X"], t["Wgu"], t["Wd"], saved, ws=ws), ws) == 6
     finally:
         api.swiglu_mlp_inject_stall_once(False)
         api.swiglu_mlp_set_wait_limit_ns(old)
@@ -409,8 +409,8 @@ def test_nograd_fused_unraised_flag_times_out_cleanly():
     old = api.swiglu_mlp_set_wait_limit_ns(20_000_000)  # 20 ms
     try:
         api.swiglu_mlp_inject_stall_once(True)
-        api.swiglu_mlp_fwd_nograd(t["X"], t["Wgu"], t["Wd"], ws=ws)
-        assert api.swiglu_mlp_query_error(ws) == 6
+        assert device_status(
+            lambda: api.swiglu_mlp_fwd_nograd(t["X"], t["Wgu"], t["Wd"], ws=ws), ws) == 6
         Y, A = api.swiglu_mlp_fwd_nograd(t["X"], t["Wgu"], t["Wd"])
         torch.cuda.synchronize()
     finally:
