@@ -236,7 +236,8 @@ def _kernel_flops(name, M, D, H):
 def _time_training(api, w, dtype_name, steps, warmup, seed, device, profile=False,
                    minimal_ws=False):
     """Times `steps` fwd+bwd steps (CUDA events on the launching stream);
-    returns (seconds per step, kernel launches, per-kernel profile, buffers).
+    returns (mean seconds per step, kernel launches, per-kernel profile,
+    buffers, median seconds per step).
 
     With profile=True a second pass of the same number of steps runs with the
     library's per-kernel events; they sit between the kernels and so launch
@@ -252,14 +253,16 @@ def _time_training(api, w, dtype_name, steps, warmup, seed, device, profile=Fals
         _step(api, t, o)
     torch.cuda.synchronize()
     st = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event after each step (a marker on the same stream: no extra sync)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     launches = 0
-    e0.record(st)
-    for _ in range(steps):
+    ev[0].record(st)
+    for i in range(steps):
         launches += _step(api, t, o)
-    e1.record(st)
+        ev[i + 1].record(st)
     torch.cuda.synchronize()
-    sec = e0.elapsed_time(e1) / 1e3 / steps
+    sec = ev[0].elapsed_time(ev[-1]) / 1e3 / steps
+    med = statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(steps)) / 1e3
     prof = None
     if profile:
         api.swiglu_mlp_profile_read()
@@ -269,7 +272,7 @@ def _time_training(api, w, dtype_name, steps, warmup, seed, device, profile=Fals
         torch.cuda.synchronize()
         api.swiglu_mlp_profile_enable(False)
         prof = api.swiglu_mlp_profile_read()
-    return sec, launches, prof, (t, o)
+    return sec, launches, prof, (t, o), med
 
 
 def _e2e(api, t, o, steps):
@@ -453,7 +456,7 @@ def _memory_report(api, w, device):
             "ws_min_MiB": round(least * mib, 3), "total_MiB": round((saved + full) * mib, 1),
             "total_min_ws_MiB": round((saved + least) * mib, 1),
             "pages_MB": {"fused": flash, "liger": liger}}
-    sec, _, _, keep = _time_training(api, w, "bf16", 10, 3, 0, device, minimal_ws=True)
+    sec, _, _, keep, _ = _time_training(api, w, "bf16", 10, 3, 0, device, minimal_ws=True)
     del keep
     torch.cuda.empty_cache()
     return {"intermediates": rows, "unit_note": "MiB = 2^20 bytes; the pages print MB",
@@ -535,7 +538,7 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    sec, launches, prof, (t, o) = _time_training(api, w, "bf16", args.steps, args.warmup,
+    sec, launches, prof, (t, o), med = _time_training(api, w, "bf16", args.steps, args.warmup,
                                                  seed=rank, device=device, profile=True)
     clocks = sampler.stop()
     flops = metrics.fwd_bwd_flops(M, D, H)
@@ -561,6 +564,7 @@ def run_ours(args):
     line = {"metric": "SwiGLU MLP fwd+bwd TFLOPS (18*M*D*H)", "value": value, "unit": "TFLOPS",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step_median": med * 1e3,
             "vs_baseline": value / world / PAGES_TFLOPS[args.workload]
             if args.workload in PAGES_TFLOPS else None,
             "dtype": "bf16", "data": "synthetic (seeded, device generator)",
@@ -597,14 +601,15 @@ def run_ours(args):
                            ("B8_S4096_D2048_H5632", ["bf16", "f16"], 25)):
             for dn in dts:
                 time.sleep(1.0)
-                s2, _, prof2, keep = _time_training(api, WORKLOADS[wl], dn, n, 10, 0, device,
+                s2, _, prof2, keep, med2 = _time_training(api, WORKLOADS[wl], dn, n, 10, 0, device,
                                                     profile=True)
                 del keep
                 w2 = WORKLOADS[wl]
                 M2, D2, H2 = w2["B"] * w2["S"], w2["D"], w2["H"]
                 f2 = metrics.fwd_bwd_flops(M2, D2, H2)
                 extra["%s_%s" % (wl, dn)] = {
-                    "ms_per_step": round(s2 * 1e3, 3), "TFLOPS": round(f2 / s2 / 1e12, 1),
+                    "ms_per_step": round(s2 * 1e3, 3), "ms_per_step_median": round(med2 * 1e3, 3),
+                    "TFLOPS": round(f2 / s2 / 1e12, 1),
                     "kernel_ms": {k: round(v[1] / v[0], 4) for k, v in prof2.items()}}
                 torch.cuda.empty_cache()
         line["other_workloads"] = extra

@@ -22,8 +22,8 @@ def test_e2e_leg_counts_its_copies_and_matches_the_device_step():
     import bench
     w = {"B": 2, "S": 128, "D": 256, "H": 512}
     M, D, H = 256, 256, 512
-    sec, launches, _, (t, o) = bench._time_training(api, w, "bf16", 2, 3, 0, "cuda:0")
-    assert sec > 0 and launches == 2 * 6  # two steps of six GEMMs
+    sec, launches, _, (t, o), med = bench._time_training(api, w, "bf16", 2, 3, 0, "cuda:0")
+    assert sec > 0 and med > 0 and launches == 2 * 6  # two steps of six GEMMs
     Y_dev, dX_dev = o["Y"].clone(), o["dX"].clone()
     e2e_sec, h2d, d2h, idle = bench._e2e(api, t, o, 3)
     assert e2e_sec > 0 and idle["h2d"] > 0 and idle["d2h"] > 0
