@@ -17,8 +17,8 @@
 //               MMAs and commits to both CTAs' "empty" / "accumulator full"
 //               barriers;
 //   warps 2..9  epilogue of this CTA's 128 rows (the epilogues of
-//               tc_gemm.cuh, unchanged); one arrival per warp on the even
-//               CTA's "accumulator empty" barrier.
+//               tc_gemm.cuh, or the TMA dG/dU form below); one arrival per
+//               warp on the even CTA's "accumulator empty" barrier.
 // Tiles (and the stream-K shares of the hybrid) are handed out per cluster.
 #pragma once
 

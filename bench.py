@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -56,12 +57,22 @@ def _peaks():
             "source": "fallback"}
 
 
+def _strip_comments(src: str) -> str:
+    """C/CUDA source without its comments and blank lines (string literals in
+    these sources hold no comment markers)."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(ln.rstrip() for ln in src.splitlines() if ln.strip())
+
+
 def _csrc_hash() -> str:
+    """Hash of the kernel sources' code (comments excluded), which keys the
+    committed ncu traffic figures to the kernels they were taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "backward_tcgen05_tma_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 
