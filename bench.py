@@ -411,7 +411,10 @@ def _nograd_sweep(api, device, peaks, sizes=NOGRAD_S):
         res.append({"S": S, "us": round(tmed * 1e6, 2), "GBps": round(byts / tmed / 1e9, 1),
                     "hbm_frac": round(byts / tmed / 1e9 / peaks["hbm_gbs"], 4),
                     "TFLOPS": round(metrics.fwd_flops(S, D, H) / tmed / 1e12, 2),
-                    "kernel_us": kern, **loop})
+                    "kernel_us": kern, **loop,
+                    # the same bytes per call in the back-to-back loop (host wall clock)
+                    "loop_hbm_frac": round(byts / (loop["loop_us_direct"] * 1e-6) / 1e9
+                                           / peaks["hbm_gbs"], 4)})
     return {"workload": "B1_D4096_H11008_bf16_nograd", "l2": "flushed (512 MiB read) before "
             "each timed call", "median_of": 20,
             "decode_loop": "%d back-to-back calls, host wall clock per call (launch cost "
