@@ -289,8 +289,10 @@ def _time_training(api, w, dtype_name, steps, warmup, seed, device, profile=Fals
 def _e2e(api, t, o, steps):
     """The same step fed from and returned to the host, as a training loop
     would run it: every step copies its X and dY from pinned host memory and
-    reads Y, dX, dWgu, dWd back into pinned host memory, all inside the timed
-    region.  The copies run on a second stream into double-buffered device
+    reads its result -- the parameter gradients dWgu, dWd, what the optimiser
+    consumes -- back into pinned host memory, all inside the timed region.
+    Y and dX stay on the device, as they do in a model, where they feed the
+    neighbouring layers.  The copies run on a second stream into double-buffered device
     slots, so step i+1's inputs arrive and step i-1's results leave while step
     i computes (the saved buffer is reused: each step's backward consumes it
     before the next forward writes it)."""
@@ -300,7 +302,7 @@ def _e2e(api, t, o, steps):
     hdy = torch.empty_like(t["dY"], device="cpu").pin_memory()
     hx.copy_(t["X"])
     hdy.copy_(t["dY"])
-    keys = ("Y", "dX", "dWgu", "dWd")
+    keys = ("dWgu", "dWd")
     slots = []
     for i in range(2):
         si = {"X": t["X"] if i == 0 else torch.empty_like(t["X"]),
@@ -361,7 +363,8 @@ def _e2e(api, t, o, steps):
 
     run(1)
     torch.cuda.synchronize()
-    idle = {"h2d": copy_gbps(slots[1][0]["X"], hx), "d2h": copy_gbps(slots[1][2]["Y"], slots[1][1]["Y"])}
+    idle = {"h2d": copy_gbps(slots[1][0]["X"], hx),
+            "d2h": copy_gbps(slots[1][2]["dWgu"], slots[1][1]["dWgu"])}
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(comp)
     run(steps)
@@ -599,11 +602,11 @@ def run_ours(args):
             "clocks": clocks,
             "e2e": {"value": flops / e2e_sec / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_sec * 1e3,
-                    "copies": "pinned host <-> device on a second stream, double-buffered "
-                              "device slots, overlapping the neighbouring steps' compute",
-                    # one 512 MiB copy each way, alone, just before the loop: the step's
-                    # 2.4 GB of copies hide behind its compute only while these stay
-                    # well above ~70 GB/s
+                    "copies": "X, dY in and the parameter gradients dWgu, dWd out (Y, dX stay "
+                              "on the device), pinned host <-> device on a second stream, "
+                              "double-buffered device slots, overlapping the neighbouring "
+                              "steps' compute",
+                    # one copy each way (X in, dWgu out), alone, just before the loop
                     "host_copy_GBps_idle": idle_copy}}
 
     if world == 1 and not args.quick:
