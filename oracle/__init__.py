@@ -77,6 +77,7 @@ def _load():
                                     dp, dp, dp, dp, dp, dp, dp]
         lib.oracle_cols.argtypes = [vp, vp, vp, vp, vp, ci, i64, i64, i64, vp, i64, ci, ci,
                                     dp, dp, dp]
+        lib.oracle_elementwise.argtypes = [i64, dp, dp, dp, dp, dp, ci, ci, cd, dp, dp, dp]
         lib.oracle_num_threads.restype = ci
         _lib = lib
         return lib
@@ -234,6 +235,40 @@ def sampled_cols(X, Wg, Wu, Wd, dY, cols, mode: int = ONE_ROUND, dt: int | None 
     lib.oracle_cols(_ptr(X), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(dY), in_dt, M, D, H,
                     _ptr(cols), C, mode, dt, _ptr(o["dWg"]), _ptr(o["dWu"]), _ptr(o["dWdT"]))
     return o
+
+
+def elementwise(dt: int, g=None, u=None, gs=None, us=None, da=None, mode: int = ONE_ROUND,
+                gate_mul: float = 1.0):
+    """The elementwise SwiGLU stage alone, on 1-D fp64 arrays of exact values.
+    Forward (g, u given): A from the sums g, u (gate multiplier applied; gs, us
+    their stored values, needed by the two-round program and defaulting to
+    rnd(g), rnd(u)).  Backward (da, gs, us given): dG, dU from dA and the
+    stored gs, us.  Returns a dict with "A" and/or "dG", "dU"."""
+    lib = _load()
+    arr = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.float64).ravel()
+    g, u, gs, us, da = arr(g), arr(u), arr(gs), arr(us), arr(da)
+    fwd = g is not None
+    bwd = da is not None
+    if fwd:
+        assert u is not None and u.size == g.size
+        gs = round_to(g, dt) if gs is None else gs
+        us = round_to(u, dt) if us is None else us
+    if bwd:
+        assert gs is not None and us is not None and gs.size == da.size == us.size
+    n = (g if fwd else da).size
+    z = np.zeros(n)
+    out = {}
+    null = ctypes.c_void_p(0)
+    if fwd:
+        out["A"] = np.empty(n)
+    if bwd:
+        out["dG"] = np.empty(n)
+        out["dU"] = np.empty(n)
+    p = lambda a: _ptr(a if a is not None else z)
+    lib.oracle_elementwise(n, p(g), p(u), p(gs), p(us), p(da), mode, dt, float(gate_mul),
+                           _ptr(out["A"]) if fwd else null, _ptr(out["dG"]) if bwd else null,
+                           _ptr(out["dU"]) if bwd else null)
+    return out
 
 
 def num_threads() -> int:

@@ -7,7 +7,10 @@
  * the seeded synthetic inputs.
  *
  * Everything is plain, slow, obviously-correct fp64 loops.  There is no
- * blocking, fusion or reordering beyond the definitions below.
+ * blocking, fusion or reordering beyond the definitions below.  Where a sum
+ * runs over the first index of a row-major matrix, the matrix is first
+ * copied transposed (values only) so that the loop reads consecutive memory;
+ * every sum still adds its terms in the order of its definition.
  *
  * What it computes (sources):
  *   "[RFC] Full-pipeline SwiGLU MLP with forward/backward co-optimization"
@@ -138,6 +141,59 @@ double oracle_dsilu(double g) {
 }
 
 /* ---------------------------------------------------------------------- */
+/* The elementwise SwiGLU stage (every form of the oracle goes through    */
+/* these two functions)                                                    */
+/* ---------------------------------------------------------------------- */
+
+/* Forward: A from the gate and up sums g, u (gate multiplier applied) and
+ * their stored values gs, us.  One-round: SiLU(g) * u in fp64 from the
+ * unrounded sums, rounded once; two-round (negative control): SiLU of the
+ * stored gate rounded first, then the product with the stored up value. */
+static double swiglu_a(double g, double u, double gs, double us, int mode, int dt) {
+  if (mode == ORACLE_TWO_ROUND) return oracle_round(oracle_round(oracle_silu(gs), dt) * us, dt);
+  return rnd(oracle_silu(g) * u, mode, dt);
+}
+
+/* Backward: from dA (never rounded) and the stored g, u,
+ *   dU = dA SiLU(g),  dG = dA u SiLU'(g) mg, each rounded once. */
+static void dswiglu(double da, double g, double u, double mg, int mode, int dt, double* dg,
+                    double* du) {
+  *du = rnd(da * oracle_silu(g), mode, dt);
+  *dg = rnd(da * u * oracle_dsilu(g) * mg, mode, dt);
+}
+
+/* The elementwise stage alone, over n elements (for checking the GPU's
+ * epilogue arithmetic on chosen values).  Forward, when A is not NULL:
+ * A[i] from g[i], u[i] (the sums, gate multiplier applied) and gs[i], us[i]
+ * (their stored values; used by the two-round program only).  Backward,
+ * when dG and dU are not NULL: dG[i], dU[i] from da[i] and the stored
+ * gs[i], us[i], with gate multiplier mg. */
+void oracle_elementwise(int64_t n, const double* g, const double* u, const double* gs,
+                        const double* us, const double* da, int mode, int dt, double mg,
+                        double* A, double* dG, double* dU) {
+  for (int64_t i = 0; i < n; ++i) {
+    if (A) A[i] = swiglu_a(g[i], u[i], gs[i], us[i], mode, dt);
+    if (dG && dU) dswiglu(da[i], gs[i], us[i], mg, mode, dt, dG + i, dU + i);
+  }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Memory layout helpers.  They move values only: every sum below adds    */
+/* its terms in the order its definition gives, whatever the layout.      */
+/* ---------------------------------------------------------------------- */
+
+/* Storage matrix [rows, cols] -> fp64 copy of its transpose [cols, rows], so
+ * that a sum over the row index reads consecutive memory. */
+static double* decode_transposed(const void* src, int dt, int64_t rows, int64_t cols) {
+  double* t = (double*)malloc((size_t)rows * (size_t)cols * sizeof(double));
+  if (!t) abort();
+#pragma omp parallel for schedule(static)
+  for (int64_t c = 0; c < cols; ++c)
+    for (int64_t r = 0; r < rows; ++r) t[c * rows + r] = load_elem(src, r * cols + c, dt);
+  return t;
+}
+
+/* ---------------------------------------------------------------------- */
 /* Full forward                                                            */
 /* ---------------------------------------------------------------------- */
 
@@ -155,14 +211,9 @@ static void gate_up_row(const void* X, const void* Wg, const void* Wu, int in_dt
     }
     g = mg * g;
     double gs = rnd(g, mode, dt), us = rnd(u, mode, dt);
-    double a;
-    if (mode == ORACLE_TWO_ROUND)
-      a = oracle_round(oracle_round(oracle_silu(gs), dt) * us, dt);
-    else
-      a = rnd(oracle_silu(g) * u, mode, dt);    /* one rounding, from unrounded g, u */
     if (Grow) Grow[j] = gs;
     if (Urow) Urow[j] = us;
-    Arow[j] = a;
+    Arow[j] = swiglu_a(g, u, gs, us, mode, dt);
   }
 }
 
@@ -203,18 +254,30 @@ void oracle_fwd(const void* X, const void* Wg, const void* Wu, const void* Wd, i
 
 /* dA[m,j] = md * sum_d dY[m,d] Wd[d,j] (kept in fp64, never rounded), then
  *   dU = dA * SiLU(G),  dG = dA * U * SiLU'(G) * mg
- * with G (= mg X Wg^T), U the stored values. */
-static void dgu_row(const void* dY, const void* Wd, int in_dt, const double* Grow,
+ * with G (= mg X Wg^T), U the stored values.  WdT is Wd transposed (fp64
+ * [H, D]): WdT[j*D + d] = Wd[d, j]. */
+static void dgu_row(const void* dY, const double* WdT, int in_dt, const double* Grow,
                     const double* Urow, int64_t m, int64_t D, int64_t H, int mode, int dt,
                     double mg, double md, double* dGrow, double* dUrow) {
   for (int64_t j = 0; j < H; ++j) {
     double da = 0.0;
-    for (int64_t d = 0; d < D; ++d)
-      da += load_elem(dY, m * D + d, in_dt) * load_elem(Wd, d * H + j, in_dt);
+    for (int64_t d = 0; d < D; ++d) da += load_elem(dY, m * D + d, in_dt) * WdT[j * D + d];
     da = md * da;
-    double g = Grow[j], u = Urow[j];
-    dUrow[j] = rnd(da * oracle_silu(g), mode, dt);
-    dGrow[j] = rnd(da * u * oracle_dsilu(g) * mg, mode, dt);
+    dswiglu(da, Grow[j], Urow[j], mg, mode, dt, dGrow + j, dUrow + j);
+  }
+}
+
+/* dX[m,k] = sum_j dG[m,j] Wg[j,k] + sum_j dU[m,j] Wu[j,k] for one row m, the
+ * two sums each over j in order; WgT, WuT: Wg, Wu transposed (fp64 [D, H]). */
+static void dx_row(const double* dGrow, const double* dUrow, const double* WgT,
+                   const double* WuT, int64_t D, int64_t H, int mode, int dt, double* dXrow) {
+  for (int64_t k = 0; k < D; ++k) {
+    double pg = 0.0, pu = 0.0;
+    for (int64_t j = 0; j < H; ++j) {
+      pg += dGrow[j] * WgT[k * H + j];
+      pu += dUrow[j] * WuT[k * H + j];
+    }
+    dXrow[k] = rnd(pg + pu, mode, dt);
   }
 }
 
@@ -230,49 +293,58 @@ void oracle_bwd_ex(const void* dY, const void* X, const void* Wg, const void* Wu
                    double mg, double md, const double* dWg0, const double* dWu0,
                    const double* dWd0, double* dG, double* dU, double* dX, double* dWg,
                    double* dWu, double* dWd) {
+  double* WdT = decode_transposed(Wd, in_dt, D, H);   /* [H, D] */
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t m = 0; m < M; ++m)
-    dgu_row(dY, Wd, in_dt, G + m * H, U + m * H, m, D, H, mode, dt, mg, md, dG + m * H,
+    dgu_row(dY, WdT, in_dt, G + m * H, U + m * H, m, D, H, mode, dt, mg, md, dG + m * H,
             dU + m * H);
+  free(WdT);
 
-  /* dWd[d,j] = md * sum_m dY[m,d] A[m,j] */
+  /* dWd[d,j] = md * sum_m dY[m,d] A[m,j]  (dYT[d*M + m] = dY[m,d], AT[j*M + m] = A[m,j]) */
+  double* dYT = decode_transposed(dY, in_dt, M, D);   /* [D, M] */
+  double* AT = decode_transposed(A, ODT_F64, M, H);   /* [H, M] */
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t d = 0; d < D; ++d)
     for (int64_t j = 0; j < H; ++j) {
       double s = 0.0;
-      for (int64_t m = 0; m < M; ++m) s += load_elem(dY, m * D + d, in_dt) * A[m * H + j];
+      for (int64_t m = 0; m < M; ++m) s += dYT[d * M + m] * AT[j * M + m];
       s = md * s;
       if (dWd0) s += dWd0[d * H + j];
       dWd[d * H + j] = rnd(s, mode, dt);
     }
+  free(dYT);
+  free(AT);
 
   /* dWg[j,k] = sum_m dG[m,j] X[m,k];  dWu[j,k] = sum_m dU[m,j] X[m,k] */
+  double* XT = decode_transposed(X, in_dt, M, D);     /* [D, M] */
+  double* dGT = decode_transposed(dG, ODT_F64, M, H); /* [H, M] */
+  double* dUT = decode_transposed(dU, ODT_F64, M, H);
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t j = 0; j < H; ++j)
     for (int64_t k = 0; k < D; ++k) {
       double sg = 0.0, su = 0.0;
       for (int64_t m = 0; m < M; ++m) {
-        double x = load_elem(X, m * D + k, in_dt);
-        sg += dG[m * H + j] * x;
-        su += dU[m * H + j] * x;
+        double x = XT[k * M + m];
+        sg += dGT[j * M + m] * x;
+        su += dUT[j * M + m] * x;
       }
       if (dWg0) sg += dWg0[j * D + k];
       if (dWu0) su += dWu0[j * D + k];
       dWg[j * D + k] = rnd(sg, mode, dt);
       dWu[j * D + k] = rnd(su, mode, dt);
     }
+  free(XT);
+  free(dGT);
+  free(dUT);
 
   /* dX[m,k] = sum_j dG[m,j] Wg[j,k] + sum_j dU[m,j] Wu[j,k] */
+  double* WgT = decode_transposed(Wg, in_dt, H, D);   /* [D, H] */
+  double* WuT = decode_transposed(Wu, in_dt, H, D);
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t m = 0; m < M; ++m)
-    for (int64_t k = 0; k < D; ++k) {
-      double pg = 0.0, pu = 0.0;
-      for (int64_t j = 0; j < H; ++j) {
-        pg += dG[m * H + j] * load_elem(Wg, j * D + k, in_dt);
-        pu += dU[m * H + j] * load_elem(Wu, j * D + k, in_dt);
-      }
-      dX[m * D + k] = rnd(pg + pu, mode, dt);
-    }
+    dx_row(dG + m * H, dU + m * H, WgT, WuT, D, H, mode, dt, dX + m * D);
+  free(WgT);
+  free(WuT);
 }
 
 /* The standard MLP, gradients overwritten. */
@@ -297,23 +369,22 @@ void oracle_rows(const void* X, const void* Wg, const void* Wu, const void* Wd,
                  double* G_s, double* U_s, double* A_s, double* Y_s,
                  double* dG_s, double* dU_s, double* dX_s) {
   (void)M;
+  double* WdT = decode_transposed(Wd, in_dt, D, H);   /* [H, D] */
+  double* WgT = decode_transposed(Wg, in_dt, H, D);   /* [D, H] */
+  double* WuT = decode_transposed(Wu, in_dt, H, D);
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < R; ++r) {
     int64_t m = rows[r];
     gate_up_row(X, Wg, Wu, in_dt, m, D, H, mode, dt, 1.0, G_s + r * H, U_s + r * H,
                 A_s + r * H);
     down_row(A_s + r * H, Wd, in_dt, D, H, mode, dt, 1.0, Y_s + r * D);
-    dgu_row(dY, Wd, in_dt, G_s + r * H, U_s + r * H, m, D, H, mode, dt, 1.0, 1.0,
+    dgu_row(dY, WdT, in_dt, G_s + r * H, U_s + r * H, m, D, H, mode, dt, 1.0, 1.0,
             dG_s + r * H, dU_s + r * H);
-    for (int64_t k = 0; k < D; ++k) {
-      double pg = 0.0, pu = 0.0;
-      for (int64_t j = 0; j < H; ++j) {
-        pg += dG_s[r * H + j] * load_elem(Wg, j * D + k, in_dt);
-        pu += dU_s[r * H + j] * load_elem(Wu, j * D + k, in_dt);
-      }
-      dX_s[r * D + k] = rnd(pg + pu, mode, dt);
-    }
+    dx_row(dG_s + r * H, dU_s + r * H, WgT, WuT, D, H, mode, dt, dX_s + r * D);
   }
+  free(WdT);
+  free(WgT);
+  free(WuT);
 }
 
 /* For the hidden units listed in cols[0..C): row j of dWg and dWu and column j
@@ -340,12 +411,8 @@ void oracle_cols(const void* X, const void* Wg, const void* Wu, const void* Wd,
       for (int64_t d = 0; d < D; ++d)
         da += load_elem(dY, m * D + d, in_dt) * load_elem(Wd, d * H + j, in_dt);
       double gs = rnd(g, mode, dt), us = rnd(u, mode, dt);
-      if (mode == ORACLE_TWO_ROUND)
-        a[m] = oracle_round(oracle_round(oracle_silu(gs), dt) * us, dt);
-      else
-        a[m] = rnd(oracle_silu(g) * u, mode, dt);
-      du[m] = rnd(da * oracle_silu(gs), mode, dt);
-      dg[m] = rnd(da * us * oracle_dsilu(gs), mode, dt);
+      a[m] = swiglu_a(g, u, gs, us, mode, dt);
+      dswiglu(da, gs, us, 1.0, mode, dt, dg + m, du + m);
     }
 #pragma omp parallel for schedule(static)
     for (int64_t d = 0; d < D; ++d) {

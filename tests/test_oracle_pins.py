@@ -73,6 +73,42 @@ def test_round_bf16_ties_and_direct_from_fp64(oracle_lib):
 
 
 # --------------------------------------------------------------------------
+# decoding the storage types: every bit pattern against library casts
+# (the inputs' values are the storage values up-converted exactly)
+# --------------------------------------------------------------------------
+
+def _same_values(got, ref):
+    """Bitwise equal as fp64 (so -0 and +0 differ), NaN compared by class."""
+    nan = np.isnan(ref)
+    np.testing.assert_array_equal(np.isnan(got), nan)
+    np.testing.assert_array_equal(got[~nan].view(np.uint64), ref[~nan].view(np.uint64))
+
+
+def test_decode_bf16_all_bit_patterns(oracle_lib):
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    t = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+    got = oracle.decode(t)
+    ref = t.to(torch.float64).numpy()
+    _same_values(got, ref)
+    # a second library route: the bf16 word is the top half of an fp32 word
+    with np.errstate(invalid="ignore"):
+        ref32 = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    _same_values(got, ref32)
+    assert np.sum(np.isinf(got)) == 2 and np.sum(np.isnan(got)) == 2 * 127
+
+
+def test_decode_f16_all_bit_patterns(oracle_lib):
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    h = bits.view(np.float16)
+    got = oracle.decode(h)
+    _same_values(got, h.astype(np.float64))
+    _same_values(got, torch.from_numpy(h.copy()).to(torch.float64).numpy())
+    # the subnormals and the normal range end where the format says
+    assert got[1] == 2.0 ** -24 and got[0x3ff] == 1023 * 2.0 ** -24 and got[0x400] == 2.0 ** -14
+    assert got[0x7bff] == 65504.0 and np.isinf(got[0x7c00]) and np.isnan(got[0x7c01])
+
+
+# --------------------------------------------------------------------------
 # SiLU and its derivative
 # --------------------------------------------------------------------------
 
@@ -323,6 +359,59 @@ def test_two_round_program_differs_substantially(oracle_lib):
     frac = float(np.mean(one["A"] != two["A"]))
     assert 0.05 < frac < 0.6, frac
     np.testing.assert_array_equal(one["G"], two["G"])
+
+
+def test_two_round_program_per_element(oracle_lib):
+    """Two-round A is rnd(rnd(SiLU(Gs)) Us) of the stored Gs, Us, element by
+    element: fp16 against numpy's direct float64 -> float16 casts, bf16 through
+    the (separately pinned) rounding; SiLU in numpy."""
+    for dtn, odt in (("f16", oracle.F16), ("bf16", oracle.BF16)):
+        t = synthetic.make_inputs(32, 256, 96, dtn, seed=9)
+        two = oracle.forward(t["X"], t["Wg"], t["Wu"], t["Wd"], mode=oracle.TWO_ROUND)
+        Gs, Us = two["G"], two["U"]
+        if dtn == "f16":
+            r = lambda v: v.astype(np.float16).astype(np.float64)
+        else:
+            r = lambda v: oracle.round_to(v, odt)
+        np.testing.assert_array_equal(two["A"], r(r(_silu_np(Gs)) * Us))
+        # and it is not the one-round value computed from the same stored Gs, Us
+        assert np.mean(two["A"] != r(_silu_np(Gs) * Us)) > 0.05
+
+
+def _one_hot_inputs(dtn, seed):
+    """X, dY one-hot rows (row m selects column m), so that every sum of the
+    MLP's contractions has one nonzero term: G[m, j] = Wg[j, m] exactly,
+    U[m, j] = Wu[j, m], dA[m, j] = Wd[m, j]."""
+    M, D, H = 24, 32, 40
+    t = synthetic.make_inputs(M, D, H, dtn, seed=seed)
+    eye = torch.zeros(M, D, dtype=t["X"].dtype)
+    eye[torch.arange(M), torch.arange(M)] = 1.0
+    t["X"] = eye
+    t["dY"] = eye.clone()
+    return t, M, D, H
+
+
+@pytest.mark.parametrize("dtn,odt", [("bf16", oracle.BF16), ("f16", oracle.F16)])
+def test_elementwise_stage_equals_full_oracle(oracle_lib, dtn, odt):
+    """oracle.elementwise (used to check the GPU's epilogue arithmetic on
+    chosen values) is the full oracle's elementwise stage: on one-hot inputs,
+    where the sums are single terms, both give the same A, dG and dU bits."""
+    t, M, D, H = _one_hot_inputs(dtn, 21)
+    f = oracle.forward(t["X"], t["Wg"], t["Wu"], t["Wd"])
+    b = oracle.backward(t["dY"], t["X"], t["Wg"], t["Wu"], t["Wd"], f)
+    g = oracle.decode(t["Wg"]).T[:M]          # G[m, j] = Wg[j, m]
+    u = oracle.decode(t["Wu"]).T[:M]
+    da = oracle.decode(t["Wd"])[:M]           # dA[m, j] = Wd[m, j]
+    np.testing.assert_array_equal(f["G"], g)
+    e = oracle.elementwise(odt, g=g, u=u)
+    np.testing.assert_array_equal(e["A"], f["A"].ravel())
+    e = oracle.elementwise(odt, gs=f["G"], us=f["U"], da=da)
+    np.testing.assert_array_equal(e["dG"], b["dG"].ravel())
+    np.testing.assert_array_equal(e["dU"], b["dU"].ravel())
+    # the two-round program goes through the same function
+    two = oracle.forward(t["X"], t["Wg"], t["Wu"], t["Wd"], mode=oracle.TWO_ROUND)
+    e = oracle.elementwise(odt, g=g, u=u, mode=oracle.TWO_ROUND)
+    np.testing.assert_array_equal(e["A"], two["A"].ravel())
 
 
 # --------------------------------------------------------------------------
