@@ -137,6 +137,10 @@ def _load(path: str) -> ctypes.CDLL:
     L.swiglu_mlp_inject_stall_once.argtypes = [ci]
     L.swiglu_mlp_last_launch_count.restype = ci
     L.swiglu_mlp_last_launch_count.argtypes = []
+    fp = ctypes.c_void_p
+    L.swiglu_mlp_test_elementwise.restype = ci
+    L.swiglu_mlp_test_elementwise.argtypes = [ci, i64, fp, fp, vp, vp, vp, fp, vp, vp, vp, vp,
+                                              ctypes.c_float, ctypes.c_float, vp]
     L.swiglu_mlp_set_cta_pairs.restype = ci
     L.swiglu_mlp_set_cta_pairs.argtypes = [ci]
     L.swiglu_mlp_set_nograd_fused.restype = ci
@@ -406,4 +410,27 @@ def swiglu_mlp_profile_read() -> dict:
     for i in range(k):
         if launches[i]:
             out[lib().swiglu_mlp_kernel_name(i).decode()] = (int(launches[i]), float(ms[i]))
+    return out
+
+
+def swiglu_mlp_test_elementwise(dtype: torch.dtype, acc_g=None, acc_u=None, dA=None, gs=None,
+                                us=None, gate_mul: float = 1.0, down_mul: float = 1.0) -> dict:
+    """Test hook: the tensor-core epilogues' elementwise stage applied to the
+    given values (1-D CUDA tensors, length a multiple of 32).  Forward from
+    fp32 accumulators acc_g, acc_u -> {"A", "G", "U"}; backward from the fp32
+    dA and the stored gs, us (``dtype``) -> {"dG", "dU"}."""
+    fwd, bwd = acc_g is not None, dA is not None
+    ref = acc_g if fwd else dA
+    n = ref.numel()
+    out = {}
+    new = lambda: torch.empty(n, dtype=dtype, device=ref.device)
+    if fwd:
+        out = {"A": new(), "G": new(), "U": new()}
+    if bwd:
+        out.update({"dG": new(), "dU": new()})
+    _check(lib().swiglu_mlp_test_elementwise(
+        dtype_code(dtype), n, _ptr(acc_g), _ptr(acc_u), _ptr(out.get("A")), _ptr(out.get("G")),
+        _ptr(out.get("U")), _ptr(dA), _ptr(gs), _ptr(us), _ptr(out.get("dG")),
+        _ptr(out.get("dU")), float(gate_mul), float(down_mul), _stream(ref.device)),
+        "swiglu_mlp_test_elementwise")
     return out

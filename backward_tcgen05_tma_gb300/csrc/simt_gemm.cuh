@@ -54,9 +54,20 @@ struct SimtEpiStore {
   }
 };
 
+// sigma(g) = 1 / (1 + e^-g) and SiLU(g) = g sigma(g) with CUDA's expf and
+// IEEE division, through t = e^-|g| (never overflows): for g < 0,
+// sigma = t / (1 + t), so SiLU stays nonzero where its fp32 value is.
+__device__ __forceinline__ float simt_sigmoid(float g) {
+  const float t = expf(-fabsf(g));
+  return g >= 0.0f ? 1.0f / (1.0f + t) : t / (1.0f + t);
+}
+__device__ __forceinline__ float simt_silu(float g) {
+  const float t = expf(-fabsf(g));
+  return g >= 0.0f ? g / (1.0f + t) : g * t / (1.0f + t);
+}
+
 // Gate/up: acc = X Wg^T, acc2 = u for hidden unit n; g = gate_mul * acc.
-// Stores G = g, U (if g != null) and A = SiLU(g) * u, SiLU(g) = g / (1 + e^-g)
-// with IEEE expf and division.
+// Stores G = g, U (if g != null) and A = SiLU(g) * u.
 struct SimtEpiSwiGLU {
   float* g;
   float* u;
@@ -74,7 +85,7 @@ struct SimtEpiSwiGLU {
       if (SWIGLU_CHECK_PTR(chk.win, ou, 4, chk.err)) *ou = uv;
     }
     float* oa = a + (int64_t)m * ld_a + n;
-    if (SWIGLU_CHECK_PTR(chk.win, oa, 4, chk.err)) *oa = gv / (1.0f + expf(-gv)) * uv;
+    if (SWIGLU_CHECK_PTR(chk.win, oa, 4, chk.err)) *oa = simt_silu(gv) * uv;
   }
 };
 
@@ -94,7 +105,7 @@ struct SimtEpiDSwiGLU {
       return;
     const float da = down_mul * acc;
     const float gv = g[o], uv = u[o];
-    const float s = 1.0f / (1.0f + expf(-gv));
+    const float s = simt_sigmoid(gv);
     u[o] = da * (gv * s);
     g[o] = da * uv * (s * (1.0f + gv * (1.0f - s)) * gate_mul);
   }

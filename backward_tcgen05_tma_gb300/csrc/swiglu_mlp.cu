@@ -1008,6 +1008,51 @@ swiglu_status simt_backward(const float* dY, const float* X, const float* Wgu, c
   return cuda_status(e);
 }
 
+// ---------------------------------------------------------------------------
+// test hook: the epilogues' elementwise stage on chosen values
+// ---------------------------------------------------------------------------
+// One thread per 32 consecutive elements (the epilogue's chunk): the forward
+// stage through swiglu_pair, the backward one through dswiglu_32, the device
+// functions the tensor-core epilogues call.
+template <bool BF16>
+__global__ void elementwise_test_kernel(int64_t chunks, const float* acc_g, const float* acc_u,
+                                        uint32_t* A, uint32_t* G, uint32_t* U, const float* dA,
+                                        const uint4* gs, const uint4* us, uint4* dG, uint4* dU,
+                                        float gate_mul, float down_mul) {
+  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= chunks) return;
+  const int64_t e0 = c * 32;
+  if (acc_g != nullptr) {
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      uint32_t a, g, u;
+      swiglu_pair<BF16>(gate_mul, acc_g[e0 + 2 * i], acc_g[e0 + 2 * i + 1], acc_u[e0 + 2 * i],
+                        acc_u[e0 + 2 * i + 1], a, g, u);
+      A[e0 / 2 + i] = a;
+      G[e0 / 2 + i] = g;
+      U[e0 / 2 + i] = u;
+    }
+  }
+  if (dA != nullptr) {
+    uint4 vg[4], vu[4];
+    uint32_t r[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      vg[q] = gs[c * 4 + q];
+      vu[q] = us[c * 4 + q];
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(dA[e0 + i]);
+    uint32_t odg[16], odu[16];
+    dswiglu_32<BF16>(vg, vu, r, gate_mul, down_mul, odg, odu);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      dG[c * 4 + q] = make_uint4(odg[4 * q], odg[4 * q + 1], odg[4 * q + 2], odg[4 * q + 3]);
+      dU[c * 4 + q] = make_uint4(odu[4 * q], odu[4 * q + 1], odu[4 * q + 2], odu[4 * q + 3]);
+    }
+  }
+}
+
 }  // namespace
 
 // ===========================================================================
@@ -1337,6 +1382,34 @@ int swiglu_mlp_profile_read(int n, int64_t* launches, double* total_ms) {
 
 const char* swiglu_mlp_kernel_name(int id) {
   return (id >= 0 && id < K_COUNT) ? kKernelNames[id] : nullptr;
+}
+
+swiglu_status swiglu_mlp_test_elementwise(swiglu_dtype dtype, int64_t n, const float* acc_g,
+                                          const float* acc_u, void* A, void* G, void* U,
+                                          const float* dA, const void* gs, const void* us,
+                                          void* dG, void* dU, float gate_multiplier,
+                                          float down_multiplier, void* stream) {
+  g_last_launches.store(0);
+  if (dtype != SWIGLU_BF16 && dtype != SWIGLU_F16) return SWIGLU_ERR_INVALID_ARG;
+  if (n < 0 || n % 32 != 0 || n > 0x7fffffffLL) return SWIGLU_ERR_INVALID_ARG;
+  const bool fwd = acc_g != nullptr, bwd = dA != nullptr;
+  if (!fwd && !bwd) return SWIGLU_ERR_INVALID_ARG;
+  swiglu_status st;
+  if (fwd && (st = check_ptrs({acc_g, acc_u, A, G, U})) != SWIGLU_OK) return st;
+  if (bwd && (st = check_ptrs({dA, gs, us, dG, dU})) != SWIGLU_OK) return st;
+  if (n == 0) return SWIGLU_OK;
+  const int64_t chunks = n / 32;
+  const int threads = 128;
+  const unsigned blocks = (unsigned)((chunks + threads - 1) / threads);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto k = dtype == SWIGLU_BF16 ? elementwise_test_kernel<true> : elementwise_test_kernel<false>;
+  k<<<blocks, threads, 0, s>>>(chunks, acc_g, acc_u, static_cast<uint32_t*>(A),
+                               static_cast<uint32_t*>(G), static_cast<uint32_t*>(U), dA,
+                               static_cast<const uint4*>(gs), static_cast<const uint4*>(us),
+                               static_cast<uint4*>(dG), static_cast<uint4*>(dU), gate_multiplier,
+                               down_multiplier);
+  g_last_launches.fetch_add(1);
+  return cuda_status(cudaGetLastError());
 }
 
 }  // extern "C"

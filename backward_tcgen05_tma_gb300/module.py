@@ -6,8 +6,8 @@ op level (``api.swiglu_mlp_fwd`` / ``_nograd`` / ``_bwd``), an autograd
 Function composing them, and a module usable in place of a transformer
 block's SwiGLU MLP (``gate_proj``, ``up_proj``, ``down_proj`` without bias).
 
-Backward overwrites the saved G/U storage with dG/dU (the page's "Known
-limitations"), so ``retain_graph=True`` followed by a second backward, and
+Backward writes dG and dU into the buffer that held G and U (the page's
+Known limitations), so ``retain_graph=True`` followed by a second backward, and
 double differentiation, are refused with an error instead of returning wrong
 values.  Every computation runs in the library's CUDA kernels; the tensors
 must be contiguous CUDA tensors of one dtype (bf16, fp16, or fp32 for the
@@ -42,8 +42,9 @@ class SwiGLUMLPFunction(torch.autograd.Function):
     @torch.autograd.function.once_differentiable
     def backward(ctx, dY):
         if ctx.consumed:
-            raise RuntimeError("SwiGLUMLPFunction: backward already ran and overwrote the saved "
-                               "G/U storage with dG/dU; retain_graph is not supported")
+            raise RuntimeError("SwiGLUMLPFunction: backward already ran; dG and dU now occupy "
+                               "the buffer that held G and U, so a second backward is "
+                               "impossible (retain_graph is not supported)")
         ctx.consumed = True
         X2, Wgu, Wd, saved = ctx.saved_tensors
         D = X2.shape[1]

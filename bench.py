@@ -41,7 +41,7 @@ MAIN = "B8_S8192_D4096_H11008"
 # (SM120), i.e. 18 M D H / t = 50.67 TFLOPS ("Training results" table)
 PAGES_TFLOPS = {MAIN: 18.0 * 65536 * 4096 * 11008 / 1.04966 / 1e12}
 NOGRAD_S = [1, 2, 4, 8, 16, 32, 64, 128, 256]
-CPU_SAMPLE_TOKENS = 16
+CPU_SAMPLE_TOKENS = 256
 REF_STEP_TOKENS = 8
 
 
@@ -308,8 +308,11 @@ def _e2e(api, t, o, steps):
         si = {"X": t["X"] if i == 0 else torch.empty_like(t["X"]),
               "dY": t["dY"] if i == 0 else torch.empty_like(t["dY"]),
               "Wgu": t["Wgu"], "Wd": t["Wd"]}
+        # own gradient buffers per slot (they are copied out while the next
+        # step runs); Y, dX, saved and ws are shared: no step allocates
         oi = dict(o) if i == 0 else {**{k: torch.empty_like(o[k]) for k in keys},
-                                     "saved": o["saved"], "ws": o["ws"]}
+                                     "Y": o["Y"], "dX": o["dX"], "saved": o["saved"],
+                                     "ws": o["ws"]}
         host = {k: torch.empty_like(o[k], device="cpu").pin_memory() for k in keys}
         slots.append((si, oi, host))
     h2d = hx.numel() * hx.element_size() + hdy.numel() * hdy.element_size()

@@ -16,7 +16,7 @@
  *   Wd  [D, H]
  *   Y   [M, D]
  *   saved [M, 3H]    one contiguous buffer holding, per token row, [G | U | A]
- *                    ("store A, G and U in one contiguous buffer", Summary)
+ *                    (Summary: the three saved activations share one buffer)
  *   dWgu [2H, D]     [dWg; dWu] in the layout of Wgu
  *   dWd [D, H],  dX [M, D],  dY [M, D]
  *
@@ -151,7 +151,7 @@ swiglu_status swiglu_mlp_fwd_nograd(const void* X, const void* Wgu, const void* 
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
  * first call before any stream capture.  Every call clears the error word
  * and counters in the array (an asynchronous memset, no allocation) and then
- * launches the two kernels.  All calls share the one array: calls that
+ * launches the kernels (one fused kernel or two).  All calls share the one array: calls that
  * overlap on the GPU (other streams, other threads) race and give undefined
  * results.  Device errors are not reported through a workspace; use
  * swiglu_mlp_fwd_nograd when they must be queried. */
@@ -195,17 +195,18 @@ swiglu_status swiglu_mlp_graph_launch(swiglu_mlp_graph* graph, void* stream);
 swiglu_status swiglu_mlp_graph_destroy(swiglu_mlp_graph* graph);
 
 /* Backward.  Consumes ``saved`` as written by swiglu_mlp_fwd on the same
- * X, Wgu, Wd: the expired G/U columns are overwritten in place with dG/dU
- * ("Summary": overwrite expired G/U storage with dG/dU; "Known limitations":
- * hence no retain_graph and no second backward on the same buffer -- a second
- * call on the same ``saved`` gives undefined values).
+ * X, Wgu, Wd: once G and U have been read they are no longer needed, and dG,
+ * dU are written over them in place (Summary; Known limitations: for that
+ * reason the graph cannot be retained and a second backward on the same
+ * buffer is not possible -- a second call on the same ``saved`` gives
+ * undefined values).
  *   dA = dY Wd is never stored: dU = dA * SiLU(G), dG = dA * U * SiLU'(G)
  *   with SiLU'(g) = s (1 + g (1 - s)), s = 1 / (1 + e^-g), G, U the stored
  *   values;
- *   dWd = dY^T A;  [dWg; dWu] = [dG | dU]^T X in one GEMM ("aggregate the dWg
- *   and dWu computations into one GEMM");  dX = [dG | dU] [Wg; Wu] with one
- *   accumulator over K = 2H ("compute dI in one fused kernel with a single
- *   accumulator").
+ *   dWd = dY^T A;  [dWg; dWu] = [dG | dU]^T X as one GEMM over the
+ *   concatenated [dG | dU] (Summary: the two weight gradients are computed
+ *   together);  dX = [dG | dU] [Wg; Wu], both halves summed in one fp32
+ *   accumulator over K = 2H (Summary: the input gradient in one kernel).
  * Gradients are written, not accumulated (beta = 0).  Writes dX [M,D],
  * dWgu [2H,D], dWd [D,H]; rewrites columns [0, 2H) of ``saved``. */
 swiglu_status swiglu_mlp_bwd(const void* dY, const void* X, const void* Wgu, const void* Wd,
@@ -336,6 +337,31 @@ int swiglu_mlp_profile_read(int n, int64_t* launches, double* total_ms);
 
 /* Name of a kernel id (NULL outside 0 .. count-1). */
 const char* swiglu_mlp_kernel_name(int id);
+
+/* Test hook: the elementwise SwiGLU stage of the tensor-core epilogues,
+ * applied by the same device functions to n caller-chosen values, so that
+ * its fp32 arithmetic can be checked value by value ("Scope one-round FP32
+ * SwiGLU to the exact Qwen3.5 contract", xorl PR #51, review section: SiLU
+ * and the product in fp32, one rounding; "[RFC] Full-pipeline SwiGLU MLP
+ * with forward/backward co-optimization", Liger-Kernel #1347, "Summary":
+ * dG and dU from dA in registers).  dtype: SWIGLU_BF16 or SWIGLU_F16.
+ *   Forward, when acc_g is not NULL: acc_g, acc_u are fp32 [n] (the gate
+ *   and up accumulators); with g = gate_multiplier * acc_g it writes
+ *   A = rnd(SiLU(g) acc_u), G = rnd(g), U = rnd(acc_u) ([n] each, dtype).
+ *   Backward, when dA is not NULL: dA is fp32 [n] (the dY Wd accumulator),
+ *   gs, us are the stored G, U ([n], dtype); it writes
+ *   dU = rnd(down_multiplier dA SiLU(gs)) and
+ *   dG = rnd(down_multiplier dA us SiLU'(gs) gate_multiplier) ([n], dtype).
+ * All pointers are device pointers, 16-byte aligned; outputs of the unused
+ * direction may be NULL.  n must be a multiple of 32 (the epilogue's
+ * chunk), 0 <= n < 2^31.  Asynchronous on ``stream``.  Errors:
+ * SWIGLU_ERR_INVALID_ARG (bad dtype, n, NULL input/output of a requested
+ * direction, or neither direction), SWIGLU_ERR_ALIGNMENT, SWIGLU_ERR_CUDA. */
+swiglu_status swiglu_mlp_test_elementwise(swiglu_dtype dtype, int64_t n, const float* acc_g,
+                                          const float* acc_u, void* A, void* G, void* U,
+                                          const float* dA, const void* gs, const void* us,
+                                          void* dG, void* dU, float gate_multiplier,
+                                          float down_multiplier, void* stream);
 
 #ifdef __cplusplus
 }

@@ -257,28 +257,70 @@ def test_stalled_tma_dgu_kernel_times_out_cleanly():
 
 
 # --------------------------------------------------------------------------
-# full-size workloads: sampled rows and hidden units against the oracle
+# full-size workloads against the oracle: B=8 S=2048 D=1024 H=2816 in full,
+# the larger ones on sampled token rows and hidden units
 # --------------------------------------------------------------------------
-FULL = [
-    ("bf16", 8, 2048, 1024, 2816),
+SAMPLED = [
     ("bf16", 8, 4096, 2048, 5632),
     ("f16", 8, 4096, 2048, 5632),
     ("bf16", 8, 8192, 4096, 11008),
 ]
 
 
-@pytest.mark.parametrize("dtn,B,S,D,H", FULL)
+def _full_size_gpu(t, H):
+    Y, saved = api.swiglu_mlp_fwd(t["X"], t["Wgu"], t["Wd"])
+    fwd = saved.clone()
+    dX, dWgu, dWd = api.swiglu_mlp_bwd(t["dY"], t["X"], t["Wgu"], t["Wd"], saved)
+    torch.cuda.synchronize()
+    return Y, fwd, saved, dX, dWgu, dWd
+
+
+@pytest.mark.slow
+def test_full_size_full_oracle_b8_s2048_d1024_h2816():
+    """Every element of every output at B=8 S=2048 D=1024 H=2816 (bf16)
+    against the full oracle (18 M D H fp64 multiply-adds, about a minute)."""
+    M, D, H = 8 * 2048, 1024, 2816
+    t = synthetic.make_inputs(M, D, H, "bf16", seed=0, device="cuda", kind="device")
+    Y, fwd, saved, dX, dWgu, dWd = _full_size_gpu(t, H)
+    g = {"Y": f64(Y), "G": f64(fwd[:, :H]), "U": f64(fwd[:, H:2 * H]), "A": f64(fwd[:, 2 * H:]),
+         "dG": f64(saved[:, :H]), "dU": f64(saved[:, H:2 * H]), "dX": f64(dX),
+         "dWg": f64(dWgu[:H]), "dWu": f64(dWgu[H:]), "dWd": f64(dWd)}
+    del fwd, saved
+    check_all(g, run_oracle(t, "bf16"), "bf16")
+
+
+def sample_rows(M, seed):
+    """256 seeded token rows, the rows at 128- and 256-row tile seams, the last
+    row, and 32 seeded rows in [0, 4096): the first 16 row tiles, where the
+    first tiles of the raster order (the stream-K-shared ones, when a GEMM
+    shares any) lie."""
+    rng = np.random.default_rng(seed)
+    seams = [0, 127, 128, 255, 256, 383, 384, 511, 512, 4095, 4096, M - 1]
+    return np.unique(np.concatenate([seams, rng.choice(M, 256, replace=False),
+                                     rng.choice(min(M, 4096), 32, replace=False)]))
+
+
+def sample_units(H, seed):
+    """128 seeded hidden units, the unit-tile seams and the last unit, and 16
+    seeded units among the first 4096 (the first weight-gradient tiles)."""
+    rng = np.random.default_rng(seed)
+    seams = [0, 63, 64, 127, 128, 255, 256, 511, 512, H - 1]
+    return np.unique(np.concatenate([[x for x in seams if x < H],
+                                     rng.choice(H, 128, replace=False),
+                                     rng.choice(min(H, 4096), 16, replace=False)]))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("dtn,B,S,D,H", SAMPLED)
 def test_full_size_sampled_parity(dtn, B, S, D, H):
     M = B * S
     t = synthetic.make_inputs(M, D, H, dtn, seed=0, device="cuda", kind="device")
-    Y, saved = api.swiglu_mlp_fwd(t["X"], t["Wgu"], t["Wd"])
-    rng = np.random.default_rng(M + D)
-    rows = np.unique(np.concatenate([[0, 127, 128, M - 1], rng.choice(M, 12, replace=False)]))
-    cols = np.unique(np.concatenate([[0, 127, 128, H - 1], rng.choice(H, 4, replace=False)]))
+    rows = sample_rows(M, M + D)
+    cols = sample_units(H, M + H)
     rt = torch.from_numpy(rows).cuda()
-    fwd_rows = saved.index_select(0, rt).cpu()
-    dX, dWgu, dWd = api.swiglu_mlp_bwd(t["dY"], t["X"], t["Wgu"], t["Wd"], saved)
-    torch.cuda.synchronize()
+    Y, fwd, saved, dX, dWgu, dWd = _full_size_gpu(t, H)
+    fwd_rows = fwd.index_select(0, rt).cpu()
+    del fwd
     bwd_rows = saved.index_select(0, rt).cpu()
     c = {k: t[k].cpu() for k in ("X", "Wg", "Wu", "Wd", "dY")}
     r = oracle.sampled_rows(c["X"], c["Wg"], c["Wu"], c["Wd"], c["dY"], rows, dt=ODT[dtn])
@@ -296,6 +338,10 @@ def test_full_size_sampled_parity(dtn, B, S, D, H):
     e = oracle.rel_frob(f64(dWgu[:H][ct]), q["dWg"]); assert e <= TOL[dtn], ("dWg", e)
     e = oracle.rel_frob(f64(dWgu[H:][ct]), q["dWu"]); assert e <= TOL[dtn], ("dWu", e)
     e = oracle.rel_frob(f64(dWd[:, ct].t()), q["dWdT"]); assert e <= TOL[dtn], ("dWd", e)
+    # the sampled rows and units each on their own: no tile is worse than the bound
+    for k in ("Y", "dX"):
+        per_row = [oracle.rel_frob(got[k][i], r[k][i]) for i in range(len(rows))]
+        assert max(per_row) <= 2 * TOL[dtn], (k, rows[int(np.argmax(per_row))], max(per_row))
 
 
 @pytest.mark.parametrize("S", [1, 2, 16, 64, 256])

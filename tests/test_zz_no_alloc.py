@@ -4,8 +4,9 @@ Some callers cannot allocate device memory -- code running under CUDA-graph
 capture, plug-ins whose host framework owns all device memory, decode loops
 that must not call cudaMalloc -- so this entry point takes no workspace and
 keeps its scratch in a static device array inside the library.  This file
-checks, through the C ABI, that two calls in a row give the same outputs as
-the workspace entry point (within the parity tolerance), and that shapes
+checks, through the C ABI, that two calls in a row give bit for bit the
+outputs of the workspace entry point (they run the same kernels), with the
+array left dirty by a call on other inputs before them, and that shapes
 beyond the array's limit are refused without a launch.  It is collected last
 so that a failure here never hides the other tests' results."""
 import ctypes
@@ -34,8 +35,9 @@ def _rel(got, ref):
 
 
 def _noalloc(L, t, M, D, H, dt):
-    Y = torch.empty(M, D, dtype=t["X"].dtype, device="cuda")
-    A = torch.empty(M, H, dtype=t["X"].dtype, device="cuda")
+    # outputs start as NaN: every element must be written by the call
+    Y = torch.full((M, D), float("nan"), dtype=t["X"].dtype, device="cuda")
+    A = torch.full((M, H), float("nan"), dtype=t["X"].dtype, device="cuda")
     rc = L.swiglu_mlp_fwd_nograd_noalloc(
         ctypes.c_void_p(t["X"].data_ptr()), ctypes.c_void_p(t["Wgu"].data_ptr()),
         ctypes.c_void_p(t["Wd"].data_ptr()), ctypes.c_void_p(Y.data_ptr()),
@@ -52,12 +54,18 @@ def test_noalloc_matches_workspace_entry_point(L, dtn, M, D, H):
     dt = {"bf16": 0, "f16": 1}[dtn]
     t = synthetic.make_inputs(M, D, H, dtn, seed=M, device="cuda", kind="device")
     Y_ref, A_ref = api.swiglu_mlp_fwd_nograd(t["X"], t["Wgu"], t["Wd"])
+    # a call on other inputs first leaves its partial sums, counters and ready
+    # bits in the array; the calls checked below must not see any of them
+    other = synthetic.make_inputs(M, D, H, dtn, seed=M + 1000, device="cuda", kind="device")
+    rc, Y_o, _ = _noalloc(L, other, M, D, H, dt)
+    assert rc == 0, api.status_string(rc)
     for _ in range(2):  # the array keeps the previous call's contents
         rc, Y, A = _noalloc(L, t, M, D, H, dt)
         assert rc == 0, api.status_string(rc)
         torch.cuda.synchronize()
-        assert _rel(Y, Y_ref) <= TOL
-        assert _rel(A, A_ref) <= TOL
+        assert torch.equal(Y, Y_ref) and torch.equal(A, A_ref)
+    assert not torch.equal(Y_o, Y_ref)
+    assert _rel(Y, Y_ref) <= TOL
 
 
 def test_noalloc_rejects_sizes_beyond_its_range(L):
