@@ -433,9 +433,10 @@ template <int AM, int BMODE, bool BF16, class Epi>
 cudaError_t launch_tc2(int kid, const CUtensorMap& ta, const CUtensorMap& tb, const TcShape& s,
                        const typename Epi::Params& ep, cudaStream_t st,
                        const CUtensorMap* tg = nullptr, const CUtensorMap* tu = nullptr) {
-  // the TMA dG/dU epilogue's slots take the room of one ring stage
+  // the TMA dG/dU epilogue's slots (GU_SLOTS x 4 KB per epilogue warp) take
+  // the room of GU_SLOTS - 1 ring stages
   constexpr bool gu = epi_tma_gu<Epi>::value;
-  constexpr int stages = gu ? TC2_STAGES - 1 : TC2_STAGES;
+  constexpr int stages = gu ? TC2_STAGES + 1 - GU_SLOTS : TC2_STAGES;
   auto kern = tc2_gemm_kernel<stages, AM, BMODE, BF16, Epi>;
   constexpr int smem = Tc2Smem<stages, gu>::DYN_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -84,10 +84,25 @@ struct epi_tma_gu<E, decltype((void)E::TMA_GU)> {
   static constexpr bool value = E::TMA_GU;
 };
 
+// Wait until at most n of this thread's committed bulk groups still read
+// shared memory (n clamped to the GU_SLOTS - 1 the pipeline can need).
+__device__ __forceinline__ void bulk_wait_group_read_n(int n) {
+  static_assert(GU_SLOTS <= 4, "bulk_wait_group_read_n covers up to 3 pending groups");
+  if (n <= 0)
+    bulk_wait_group_read<0>();
+  else if (n == 1)
+    bulk_wait_group_read<1>();
+  else if (n == 2)
+    bulk_wait_group_read<2>();
+  else
+    bulk_wait_group_read<3>();
+}
+
 // One epilogue warp's stream of G/U jobs: job k (one 32 x 32 chunk) uses
-// slot k % GU_SLOTS and that slot's barrier phase (k / GU_SLOTS) & 1.  The
-// issue cursor walks the chunks of a tile (row0, col0), then of the next
-// tile if it is known to run its epilogue.
+// slot k % GU_SLOTS and that slot's barrier phase (k / GU_SLOTS) & 1.  Each
+// job commits one bulk group of stores (empty when nothing is stored), so
+// group k belongs to job k.  The issue cursor walks the chunks of a tile
+// (row0, col0), then of the next tile if it is known to run its epilogue.
 struct GuPipe {
   uint32_t slot0, bar0;      // slot 0's shared address and barrier
   uint32_t issued, done;     // jobs whose loads were issued / whose stores were issued
@@ -100,9 +115,14 @@ struct GuPipe {
                                              const CUtensorMap* um, int lane) {
     while (issued <= kmax && cur_c < GU_CHUNKS) {
       const uint32_t b = issued % GU_SLOTS;
+      if (lane == 0 && issued >= (uint32_t)GU_SLOTS) {
+        // the slot's previous job, issued - GU_SLOTS, must have finished
+        // reading its dG/dU out of the slot; the groups committed after its
+        // own (done - 1 - (issued - GU_SLOTS) of them) may still be reading
+        const int prev = (int)issued - GU_SLOTS;
+        if (prev < (int)done) bulk_wait_group_read_n((int)done - 1 - prev);
+      }
       if (lane == 0) {
-        // the slot's previous job stored from it one chunk or more ago
-        bulk_wait_group_read<0>();
         const uint32_t bar = bar0 + 8u * b, dst = slot0 + GU_SLOT_BYTES * b;
         mbar_arrive_expect_tx(bar, GU_SLOT_BYTES);
         tma_load_2d(dst, gm, bar, cur_col0 + cur_c * 32, cur_row0);

@@ -617,20 +617,31 @@ def run_ours(args):
         # each timed over about 100 ms after a pause and a warm-up, so that the
         # short steps are not measured while the clocks recover from the
         # power-capped main workload
-        for wl, dts, n in (("B8_S2048_D1024_H2816", ["bf16"], 150),
-                           ("B8_S4096_D2048_H5632", ["bf16", "f16"], 25)):
+        # each timed over about 1 s after a pause and a warm-up, so that the
+        # short steps are not measured while the clocks recover from the
+        # power-capped main workload, with the SM clock sampled meanwhile
+        # (TFLOPS per GHz compares dtypes whose clocks differ under the cap)
+        for wl, dts, n in (("B8_S2048_D1024_H2816", ["bf16"], 1500),
+                           ("B8_S4096_D2048_H5632", ["bf16", "f16"], 220)):
             for dn in dts:
                 time.sleep(1.0)
+                cs = ClockSampler(local)
+                cs.start()
                 s2, _, prof2, keep, med2 = _time_training(api, WORKLOADS[wl], dn, n, 10, 0, device,
                                                     profile=True)
+                ck = cs.stop()
                 del keep
                 w2 = WORKLOADS[wl]
                 M2, D2, H2 = w2["B"] * w2["S"], w2["D"], w2["H"]
                 f2 = metrics.fwd_bwd_flops(M2, D2, H2)
+                tf = f2 / s2 / 1e12
                 extra["%s_%s" % (wl, dn)] = {
                     "ms_per_step": round(s2 * 1e3, 3), "ms_per_step_median": round(med2 * 1e3, 3),
-                    "TFLOPS": round(f2 / s2 / 1e12, 1),
-                    "kernel_ms": {k: round(v[1] / v[0], 4) for k, v in prof2.items()}}
+                    "TFLOPS": round(tf, 1),
+                    "kernel_ms": {k: round(v[1] / v[0], 4) for k, v in prof2.items()},
+                    "clocks": ck,
+                    "TFLOPS_per_GHz": round(tf / (ck["sm_mhz"] / 1e3), 1)
+                    if ck.get("sm_mhz") else None}
                 torch.cuda.empty_cache()
         line["other_workloads"] = extra
         line["memory"] = _memory_report(api, w, device)
