@@ -76,7 +76,14 @@ struct NgSmem {
   static constexpr int X_BYTES = NT * 64 * 2;   // the tokens' k-block
   static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
   static constexpr int USTAGE_BYTES = 64 * NT * 4;  // U rows of a whole gate/up tile
-  static constexpr int STAGES = (200 * 1024 - USTAGE_BYTES) / STAGE_BYTES;
+  // ~110 KB of ring (5 stages at 16 and 32 tokens, 4 at 64): single L2-flushed
+  // calls at D = 4096, H = 11008 measured 62.1 vs 64.2 us (1-16 tokens) and
+  // 68.2 vs 74.4 us (32 tokens) against a ~200 KB ring, with the same bits;
+  // the extra bytes in flight only queued behind the other SMs' requests.
+  // (Two CTAs per SM -- this ring with registers capped so that the down
+  // kernel's CTAs sit beside gate/up's from the start -- was slower still.)
+  static constexpr int STAGES_FIT = (110 * 1024 - USTAGE_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT < 4 ? 4 : STAGES_FIT;
   static constexpr int USTAGE_OFFSET = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFFSET = USTAGE_OFFSET + USTAGE_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, acc_full[2], acc_empty[2], drain
