@@ -35,6 +35,10 @@ WORKLOADS = {
     "B8_S8192_D4096_H11008": dict(B=8, S=8192, D=4096, H=11008),
     "B8_S4096_D2048_H5632": dict(B=8, S=4096, D=2048, H=5632),
     "B8_S2048_D1024_H2816": dict(B=8, S=2048, D=1024, H=2816),
+    # the main workload's layer at 1/8 and 1/4 of its tokens: small enough for
+    # multi-metric ncu captures, from which its per-launch traffic is scaled
+    "B1_S8192_D4096_H11008": dict(B=1, S=8192, D=4096, H=11008),
+    "B2_S8192_D4096_H11008": dict(B=2, S=8192, D=4096, H=11008),
 }
 MAIN = "B8_S8192_D4096_H11008"
 # the pages' own number for this workload: 1049.66 ms on an RTX 5060 Ti
