@@ -1027,8 +1027,13 @@ __global__ void elementwise_test_kernel(int64_t chunks, const float* acc_g, cons
 #pragma unroll 4
     for (int i = 0; i < 16; ++i) {
       uint32_t a, g, u;
-      swiglu_pair<BF16>(gate_mul, acc_g[e0 + 2 * i], acc_g[e0 + 2 * i + 1], acc_u[e0 + 2 * i],
-                        acc_u[e0 + 2 * i + 1], a, g, u);
+      // the branch the gate/up epilogue takes for this multiplier
+      if (gate_mul == 1.0f)
+        swiglu_pair<BF16, false>(gate_mul, acc_g[e0 + 2 * i], acc_g[e0 + 2 * i + 1],
+                                 acc_u[e0 + 2 * i], acc_u[e0 + 2 * i + 1], a, g, u);
+      else
+        swiglu_pair<BF16>(gate_mul, acc_g[e0 + 2 * i], acc_g[e0 + 2 * i + 1], acc_u[e0 + 2 * i],
+                          acc_u[e0 + 2 * i + 1], a, g, u);
       A[e0 / 2 + i] = a;
       G[e0 / 2 + i] = g;
       U[e0 / 2 + i] = u;

@@ -335,12 +335,13 @@ struct EpiStore {
 // accumulators acc_g = X Wg^T and acc_u = X Wu^T: with g = gate_mul acc_g,
 // packed G = rnd(g), U = rnd(acc_u) and A = rnd(SiLU(g) acc_u), A formed from
 // the unrounded values and rounded once.
-template <bool BF16>
+// MUL = false: gate_mul is 1 and its multiply is left out (the same bits).
+template <bool BF16, bool MUL = true>
 __device__ __forceinline__ void swiglu_pair(float gate_mul, float acc_g0, float acc_g1,
                                             float acc_u0, float acc_u1, uint32_t& a,
                                             uint32_t& g, uint32_t& u) {
   using P = Pack<BF16>;
-  const float g0 = gate_mul * acc_g0, g1 = gate_mul * acc_g1;
+  const float g0 = MUL ? gate_mul * acc_g0 : acc_g0, g1 = MUL ? gate_mul * acc_g1 : acc_g1;
   a = P::two(silu_f32(g0) * acc_u0, silu_f32(g1) * acc_u1);
   g = P::two(g0, g1);
   u = P::two(acc_u0, acc_u1);
@@ -377,11 +378,19 @@ struct EpiSwiGLU {
       tmem_ld_32x32b_x32(tacc + HALF + c * 32, ru);
       tmem_ld_wait();
       uint32_t va[16], vg[16], vu[16];
+      if (p.gate_mul == 1.0f) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        swiglu_pair<BF16>(p.gate_mul, __uint_as_float(rg[2 * i]), __uint_as_float(rg[2 * i + 1]),
-                          __uint_as_float(ru[2 * i]), __uint_as_float(ru[2 * i + 1]), va[i],
-                          vg[i], vu[i]);
+        for (int i = 0; i < 16; ++i)
+          swiglu_pair<BF16, false>(p.gate_mul, __uint_as_float(rg[2 * i]),
+                                   __uint_as_float(rg[2 * i + 1]), __uint_as_float(ru[2 * i]),
+                                   __uint_as_float(ru[2 * i + 1]), va[i], vg[i], vu[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          swiglu_pair<BF16>(p.gate_mul, __uint_as_float(rg[2 * i]), __uint_as_float(rg[2 * i + 1]),
+                            __uint_as_float(ru[2 * i]), __uint_as_float(ru[2 * i + 1]), va[i],
+                            vg[i], vu[i]);
+      }
       const int jc = j0 + c * 32;
       auto ok = [&](int q) { return jc + q * 8 + 8 <= s.N; };
       auto dst = [&](void* base, int64_t ld) {
@@ -417,11 +426,11 @@ struct EpiSwiGLU {
 // dU = rnd(dA SiLU(g)), dG = rnd(dA u SiLU'(g) gate_mul) for 32 columns of
 // one row: g, u packed in vg, vu (8 words of 2 each); r = the accumulator's
 // 32 fp32 columns (dA = down_mul r).
-template <bool BF16>
-__device__ __forceinline__ void dswiglu_32(const uint4 (&vg)[4], const uint4 (&vu)[4],
-                                           const uint32_t (&r)[32], float gate_mul,
-                                           float down_mul, uint32_t (&odg)[16],
-                                           uint32_t (&odu)[16]) {
+template <bool BF16, bool MUL>
+__device__ __forceinline__ void dswiglu_32_impl(const uint4 (&vg)[4], const uint4 (&vu)[4],
+                                                const uint32_t (&r)[32], float gate_mul,
+                                                float down_mul, uint32_t (&odg)[16],
+                                                uint32_t (&odu)[16]) {
   using P = Pack<BF16>;
 #pragma unroll
   for (int g8 = 0; g8 < 4; ++g8) {
@@ -431,16 +440,38 @@ __device__ __forceinline__ void dswiglu_32(const uint4 (&vg)[4], const uint4 (&v
     for (int e = 0; e < 4; ++e) {
       const float2 g = P::unpack(pg[e]);
       const float2 u = P::unpack(pu[e]);
-      const float da0 = down_mul * __uint_as_float(r[g8 * 8 + 2 * e]);
-      const float da1 = down_mul * __uint_as_float(r[g8 * 8 + 2 * e + 1]);
+      float da0 = __uint_as_float(r[g8 * 8 + 2 * e]);
+      float da1 = __uint_as_float(r[g8 * 8 + 2 * e + 1]);
+      if constexpr (MUL) {
+        da0 *= down_mul;
+        da1 *= down_mul;
+      }
       const float s0 = sigmoid_f32(g.x);
       const float s1 = sigmoid_f32(g.y);
-      const float ds0 = s0 * (1.0f + g.x * (1.0f - s0)) * gate_mul;
-      const float ds1 = s1 * (1.0f + g.y * (1.0f - s1)) * gate_mul;
+      float ds0 = s0 * (1.0f + g.x * (1.0f - s0));
+      float ds1 = s1 * (1.0f + g.y * (1.0f - s1));
+      if constexpr (MUL) {
+        ds0 *= gate_mul;
+        ds1 *= gate_mul;
+      }
       odu[g8 * 4 + e] = P::two(da0 * (g.x * s0), da1 * (g.y * s1));
       odg[g8 * 4 + e] = P::two(da0 * u.x * ds0, da1 * u.y * ds1);
     }
   }
+}
+
+// The standard MLP (both multipliers 1) takes a form without the two
+// multiplies, the same bits: measured 3.5% faster for the dG/dU kernel at
+// B=8 S=8192 D=4096 H=11008, and it leaves that kernel's registers unspilled.
+template <bool BF16>
+__device__ __forceinline__ void dswiglu_32(const uint4 (&vg)[4], const uint4 (&vu)[4],
+                                           const uint32_t (&r)[32], float gate_mul,
+                                           float down_mul, uint32_t (&odg)[16],
+                                           uint32_t (&odu)[16]) {
+  if (gate_mul == 1.0f && down_mul == 1.0f)
+    dswiglu_32_impl<BF16, false>(vg, vu, r, gate_mul, down_mul, odg, odu);
+  else
+    dswiglu_32_impl<BF16, true>(vg, vu, r, gate_mul, down_mul, odg, odu);
 }
 
 struct EpiDSwiGLUParams {
