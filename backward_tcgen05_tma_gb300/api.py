@@ -387,9 +387,9 @@ def swiglu_mlp_set_cta_pairs(mode: int = 1) -> int:
     return int(lib().swiglu_mlp_set_cta_pairs(int(mode)))
 
 
-def swiglu_mlp_set_nograd_fused(mode: int = 1) -> int:
-    """Few-token no-grad calls: 0 two kernels, 1 the fused kernel for 33..64
-    tokens (the default), 2 always the fused kernel; returns the previous mode."""
+def swiglu_mlp_set_nograd_fused(mode: int = 0) -> int:
+    """Few-token no-grad calls: 0 two kernels (the default), 1 the fused kernel
+    for 33..64 tokens, 2 always the fused kernel; returns the previous mode."""
     return int(lib().swiglu_mlp_set_nograd_fused(int(mode)))
 
 

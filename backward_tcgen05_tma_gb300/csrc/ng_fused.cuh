@@ -56,12 +56,17 @@ struct NgDynArgs {
   int inject_unready;  // test hook: tile 0's bit is never set, so the waits on it run out
 };
 
-// The two-kernel form's ring and staging, plus the unit queue and four TMEM
-// accumulators (the MMA warp may run up to three units ahead of the
-// epilogue, whose per-unit work includes a few L2 round trips).
+// Weight ring of the fused kernel, per SM: 200 KB measured 2 us faster than
+// 110 KB at 16-64 tokens (the two-kernel form does best with 110 KB).
+constexpr int NG_FUSED_RING_KB = 200;
+
+// The two-kernel form's ring layout (with the fused kernel's ring size) and
+// staging, plus the unit queue and four TMEM accumulators (the MMA warp may
+// run up to three units ahead of the epilogue, whose per-unit work includes
+// a few L2 round trips).
 template <int NT>
 struct NgDynSmem {
-  using B = NgSmem<NT>;
+  using B = NgSmem<NT, NG_FUSED_RING_KB>;
   static constexpr int UQ = 8;                    // unit queue entries
   static constexpr int NACC = 4;                  // TMEM accumulators
   static constexpr int UQ_BAR_OFFSET = B::TOTAL;  // uq_full[UQ], uq_empty[UQ]
@@ -102,7 +107,7 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmX,
                     const __grid_constant__ CUtensorMap tmWd,
                     const __grid_constant__ CUtensorMap tmA, const NgDynArgs f) {
-  using L = NgSmem<NT>;
+  using L = NgSmem<NT, NG_FUSED_RING_KB>;
   using Q = NgDynSmem<NT>;
   static_assert(NT == 16 || NT == 32 || NT == 64, "NT must be 16, 32 or 64");
   static_assert(Q::TOTAL + 1024 <= 232448, "shared memory plan exceeds 227 KB");

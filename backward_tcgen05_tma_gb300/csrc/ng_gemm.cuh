@@ -70,7 +70,7 @@ __device__ __forceinline__ void ng_put(const NgArgs& a, int m, int col, float v)
   }
 }
 
-template <int NT>
+template <int NT, int RING_KB = 110>
 struct NgSmem {
   static constexpr int W_BYTES = 128 * 64 * 2;  // 16 KB of weights per k-block
   static constexpr int X_BYTES = NT * 64 * 2;   // the tokens' k-block
@@ -82,7 +82,7 @@ struct NgSmem {
   // the extra bytes in flight only queued behind the other SMs' requests.
   // (Two CTAs per SM -- this ring with registers capped so that the down
   // kernel's CTAs sit beside gate/up's from the start -- was slower still.)
-  static constexpr int STAGES_FIT = (110 * 1024 - USTAGE_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES_FIT = (RING_KB * 1024 - USTAGE_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT < 4 ? 4 : STAGES_FIT;
   static constexpr int USTAGE_OFFSET = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFFSET = USTAGE_OFFSET + USTAGE_BYTES;

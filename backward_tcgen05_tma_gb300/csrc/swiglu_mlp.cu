@@ -105,7 +105,7 @@ bool take_inject() {
 }
 std::atomic<int> g_last_launches{0};
 std::atomic<int> g_cta_pairs{1};  // SM pairs (cta_group::2): 0 never, 1 by size, 2 always
-std::atomic<int> g_ng_fused{1};   // few-token no-grad: fused kernel 0 never, 1 by size, 2 always
+std::atomic<int> g_ng_fused{0};   // few-token no-grad: fused kernel 0 never, 1 for 33..64 tokens, 2 always
 constexpr int TC2_STAGES = 6;
 
 // ---------------------------------------------------------------------------

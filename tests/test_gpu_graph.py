@@ -20,23 +20,31 @@ def _built():
     api.lib()
 
 
-@pytest.mark.parametrize("dtn,M,D,H", [("bf16", 1, 4096, 11008), ("bf16", 16, 4096, 11008),
-                                       ("f16", 33, 1024, 2816), ("bf16", 64, 2048, 5632),
-                                       ("bf16", 300, 512, 392), ("f32", 32, 64, 176)])
-def test_graph_replay_equals_direct_call(dtn, M, D, H):
+@pytest.mark.parametrize("dtn,M,D,H,fused", [("bf16", 1, 4096, 11008, 0),
+                                             ("bf16", 16, 4096, 11008, 0),
+                                             ("f16", 33, 1024, 2816, 0), ("f16", 33, 1024, 2816, 2),
+                                             ("bf16", 64, 2048, 5632, 0),
+                                             ("bf16", 64, 2048, 5632, 2),
+                                             ("bf16", 300, 512, 392, 0), ("f32", 32, 64, 176, 0)])
+def test_graph_replay_equals_direct_call(dtn, M, D, H, fused):
+    """Replays equal direct calls bit for bit, for both few-token forms."""
     t = synthetic.make_inputs(M, D, H, dtn, seed=31, device="cuda", kind="device")
-    g = api.FwdNogradGraph(t["Wgu"], t["Wd"], M)
-    for step in range(3):
-        x = torch.randn(M, D, device="cuda").to(TDT[dtn])
-        y = g(x).clone()
-        n_graph = api.swiglu_mlp_last_launch_count()
-        Yd, Ad = api.swiglu_mlp_fwd_nograd(x, t["Wgu"], t["Wd"])
-        n_direct = api.swiglu_mlp_last_launch_count()
-        torch.cuda.synchronize()
-        assert torch.equal(y, Yd), step
-        assert torch.equal(g.A, Ad), step
-        assert n_graph == n_direct >= 1
-    g.close()
+    old = api.swiglu_mlp_set_nograd_fused(fused)
+    try:
+        g = api.FwdNogradGraph(t["Wgu"], t["Wd"], M)
+        for step in range(3):
+            x = torch.randn(M, D, device="cuda").to(TDT[dtn])
+            y = g(x).clone()
+            n_graph = api.swiglu_mlp_last_launch_count()
+            Yd, Ad = api.swiglu_mlp_fwd_nograd(x, t["Wgu"], t["Wd"])
+            n_direct = api.swiglu_mlp_last_launch_count()
+            torch.cuda.synchronize()
+            assert torch.equal(y, Yd), step
+            assert torch.equal(g.A, Ad), step
+            assert n_graph == n_direct >= 1
+        g.close()
+    finally:
+        api.swiglu_mlp_set_nograd_fused(old)
 
 
 def test_graph_matches_oracle():

@@ -50,7 +50,7 @@ def _noalloc(L, t, M, D, H, dt):
                                        ("bf16", 32, 4096, 11008), ("f16", 5, 320, 392),
                                        ("bf16", 32, 512, 1024), ("bf16", 64, 4096, 11008)])
 def test_noalloc_matches_workspace_entry_point(L, dtn, M, D, H):
-    # M = 33..64 runs the fused kernel by default, fewer tokens two kernels
+    # the default few-token form (two kernels) at 1 to 64 tokens
     dt = {"bf16": 0, "f16": 1}[dtn]
     t = synthetic.make_inputs(M, D, H, dtn, seed=M, device="cuda", kind="device")
     Y_ref, A_ref = api.swiglu_mlp_fwd_nograd(t["X"], t["Wgu"], t["Wd"])
