@@ -125,6 +125,12 @@ def _load(path: str) -> ctypes.CDLL:
     L.swiglu_mlp_bwd_ex.restype = ci
     L.swiglu_mlp_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, op, vp,
                                     sz, vp]
+    L.swiglu_mlp_packed_weights_bytes.restype = sz
+    L.swiglu_mlp_packed_weights_bytes.argtypes = [i64, i64, ci]
+    L.swiglu_mlp_pack_weights.restype = ci
+    L.swiglu_mlp_pack_weights.argtypes = [vp, vp, vp, i64, i64, ci, vp]
+    L.swiglu_mlp_fwd_nograd_packed.restype = ci
+    L.swiglu_mlp_fwd_nograd_packed.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, op, vp, sz, vp]
     L.swiglu_mlp_bwd.restype = ci
     L.swiglu_mlp_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp, sz, vp]
     L.swiglu_mlp_query_error.restype = ci
@@ -271,6 +277,45 @@ def swiglu_mlp_fwd_nograd_noalloc(X, Wgu, Wd, out: dict | None = None):
     _check(lib().swiglu_mlp_fwd_nograd_noalloc(_ptr(X), _ptr(Wgu), _ptr(Wd), _ptr(Y), _ptr(A), M,
                                                D, H, dtype_code(X.dtype), _stream(X.device)),
            "swiglu_mlp_fwd_nograd_noalloc")
+    return Y, A
+
+
+def swiglu_mlp_pack_weights(Wgu, Wd, packed=None) -> torch.Tensor:
+    """The packed copy of (Wgu [2H,D], Wd [D,H]) that
+    swiglu_mlp_fwd_nograd_packed streams (a uint8 device tensor)."""
+    H2, D = Wgu.shape
+    H = H2 // 2
+    if Wgu.shape != (2 * H, D) or Wd.shape != (D, H):
+        raise ValueError("expected Wgu [2H, D] and Wd [D, H]")
+    n = int(lib().swiglu_mlp_packed_weights_bytes(D, H, dtype_code(Wgu.dtype)))
+    if n == 0:
+        raise SwigluError(3, "swiglu_mlp_pack_weights")
+    packed = torch.empty(n, dtype=torch.uint8, device=Wgu.device) if packed is None else packed
+    if packed.numel() < n:
+        raise ValueError("packed buffer too small")
+    _check(lib().swiglu_mlp_pack_weights(_ptr(Wgu), _ptr(Wd), _ptr(packed), D, H,
+                                         dtype_code(Wgu.dtype), _stream(Wgu.device)),
+           "swiglu_mlp_pack_weights")
+    return packed
+
+
+def swiglu_mlp_fwd_nograd_packed(X, packed, H: int, out: dict | None = None, ws=None,
+                                 gate_mul: float = 1.0, down_mul: float = 1.0):
+    """Few-token (M <= 64) no-grad forward on weights packed by
+    swiglu_mlp_pack_weights: returns (Y [M,D], A [M,H])."""
+    M, D = X.shape
+    out = out or {}
+    Y = out.get("Y")
+    Y = torch.empty(M, D, dtype=X.dtype, device=X.device) if Y is None else Y
+    A = out.get("A")
+    A = torch.empty(M, H, dtype=X.dtype, device=X.device) if A is None else A
+    ws = workspace(M, D, H, X.dtype, SWIGLU_OP_FWD_NOGRAD, X.device) if ws is None else ws
+    _check(lib().swiglu_mlp_fwd_nograd_packed(_ptr(X), _ptr(packed), _ptr(Y), _ptr(A), M, D, H,
+                                              dtype_code(X.dtype),
+                                              _opts(gate_mul, down_mul, False), _ptr(ws),
+                                              ws.numel(), _stream(X.device)),
+           "swiglu_mlp_fwd_nograd_packed")
+    _device_check(ws, "swiglu_mlp_fwd_nograd_packed")
     return Y, A
 
 

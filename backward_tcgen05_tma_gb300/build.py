@@ -18,8 +18,6 @@ NVCC_FLAGS = [
     "-std=c++17", "-O3", "-lineinfo",
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-Xcompiler", "-fPIC", "-shared",
-    # optimise the translation unit's kernels in parallel on every host core
-    "--split-compile=0",
 ]
 
 

@@ -26,6 +26,14 @@
 // The down kernel is launched as a programmatic dependent of the gate/up
 // kernel: its CTAs start streaming Wd into the ring while gate/up drains, and
 // wait (griddepcontrol.wait) only before touching anything gate/up writes.
+//
+// Packed weights (PACKED): the weight boxes were laid out once, ahead of the
+// calls, as contiguous 16 KB blocks in the order the stream-K split consumes
+// them (tile-major, k-blocks within a tile), each already in the 128-byte
+// swizzled form the TMA box load would produce in shared memory.  A CTA's
+// range is then one contiguous region of the packed buffer, fetched with
+// plain bulk copies instead of 128-byte rows scattered over the weight
+// matrix; the shared-memory contents, and so the results, are the same.
 #pragma once
 
 #include "tc_gemm.cuh"
@@ -52,6 +60,8 @@ struct NgArgs {
   uint64_t wait_limit_ns;
   int* err;
   float scale = 1.0f;  // gate/up: gate multiplier (SiLU(scale g) u); down: Y = scale y
+  const uint8_t* wpack = nullptr;  // PACKED: this GEMM's boxes, box (tile, kb) at
+                                   //   (tile * kb_tile + kb) * 16 KB
 #ifdef SWIGLU_DEBUG
   DbgWin dbg;       // buffers the kernel may touch by plain accesses: out, workspace
 #endif
@@ -367,7 +377,7 @@ __device__ __forceinline__ bool ng_epilogue_segment(const NgArgs& a, int tile, b
 
 constexpr int NG_THREADS = 192;  // producer warp, MMA warp, 4 epilogue warps
 
-template <int NT, bool GATE_UP, bool BF16>
+template <int NT, bool GATE_UP, bool BF16, bool PACKED = false>
 __global__ void __launch_bounds__(NG_THREADS, 1)
     ng_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const NgArgs a) {
@@ -415,7 +425,7 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmW);
+    if (!PACKED) tma_prefetch_desc(&tmW);  // (with packed weights tmW is unused)
     tma_prefetch_desc(&tmX);
   }
   if (warp == 1) {
@@ -435,6 +445,16 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
   auto segs = [&]() {
     return NgSegIter{x_begin, x_end, 0, dp_count, a.kb_tile, a.sk_tiles, (int)blockIdx.x,
                      (int)gridDim.x};
+  };
+
+  // the weight box (tile, k-block kb) into the ring slot at ``slot``
+  auto load_w = [&](uint32_t slot, uint32_t bar, int tile, int kb) {
+    if (PACKED)
+      bulk_load(slot, a.wpack + ((size_t)tile * a.kb_tile + kb) * L::W_BYTES, L::W_BYTES, bar);
+    else if (GATE_UP)
+      tma_load_3d(slot, &tmW, bar, kb * TC_BK, tile * TILE_ROWS, 0);
+    else
+      tma_load_2d(slot, &tmW, bar, kb * TC_BK, tile * TILE_ROWS);
   };
 
   if (warp == 0) {
@@ -457,10 +477,7 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
             const int k0 = (kb0 + i) * TC_BK;
             const uint32_t sw = sbase + pending_x * L::STAGE_BYTES;
             mbar_arrive_expect_tx(full_bar(pending_x), L::STAGE_BYTES);
-            if (GATE_UP)
-              tma_load_3d(sw, &tmW, full_bar(pending_x), k0, tile * TILE_ROWS, 0);
-            else
-              tma_load_2d(sw, &tmW, full_bar(pending_x), k0, tile * TILE_ROWS);
+            load_w(sw, full_bar(pending_x), tile, kb0 + i);
             pending_k0[pending_x] = k0;
             issued_mask |= 1u << pending_x;
             ++pending_x;
@@ -495,10 +512,7 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
           const uint32_t sx = sw + L::W_BYTES;
           const int k0 = (kb0 + i) * TC_BK;
           mbar_arrive_expect_tx(full_bar(stage), L::STAGE_BYTES);
-          if (GATE_UP)
-            tma_load_3d(sw, &tmW, full_bar(stage), k0, tile * TILE_ROWS, 0);
-          else
-            tma_load_2d(sw, &tmW, full_bar(stage), k0, tile * TILE_ROWS);
+          load_w(sw, full_bar(stage), tile, kb0 + i);
           tma_load_2d(sx, &tmX, full_bar(stage), k0, 0);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);

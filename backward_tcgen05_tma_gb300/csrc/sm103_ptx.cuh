@@ -129,6 +129,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
+// Contiguous bulk copy global -> shared (no tensor map): `bytes` (a multiple
+// of 16, both addresses 16-byte aligned) counted on the mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // TMA tensor store, shared::cta -> global, tracked in bulk-async groups: the
 // tensor map clips the box at the tensor's bounds.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int32_t x,

@@ -482,6 +482,55 @@ cudaError_t launch_simt(int kid, SimtOperand A, SimtOperand B, SimtOperand B2, i
 }
 
 // ---------------------------------------------------------------------------
+// packed weights for the few-token no-grad forward
+// ---------------------------------------------------------------------------
+// Layout: the gate/up boxes, then the down boxes, 16 KB each.  Gate/up box
+// (t, kb), t < ceil(H/64), kb < ceil(D/64), sits at (t * ceil(D/64) + kb) * 16
+// KB: rows 0..63 are Wg rows t*64.., rows 64..127 the Wu rows of the same
+// units, 64 elements (128 bytes) of K from kb*64 each.  Down box (t, kb),
+// t < ceil(D/128), kb < ceil(H/64): Wd rows t*128.., K from kb*64.  Within a
+// box the 16-byte chunk c of row r is stored at r*128 + (c ^ (r & 7))*16 (the
+// 128-byte swizzle of the tensor-map loads); elements past D or H are zero.
+constexpr size_t PACK_BOX_BYTES = 16384;
+
+size_t packed_gateup_bytes(int64_t D, int64_t H) {
+  return (size_t)((H + 63) / 64) * (size_t)((D + 63) / 64) * PACK_BOX_BYTES;
+}
+
+size_t packed_down_bytes(int64_t D, int64_t H) {
+  return (size_t)((D + 127) / 128) * (size_t)((H + 63) / 64) * PACK_BOX_BYTES;
+}
+
+// One thread per 16-byte chunk of the packed buffer.
+__global__ void pack_weights_kernel(const uint8_t* __restrict__ Wgu, const uint8_t* __restrict__ Wd,
+                                    uint4* __restrict__ out, int64_t D, int64_t H,
+                                    int64_t gu_chunks, int64_t all_chunks) {
+  const int64_t kb1 = (D + 63) / 64, kb2 = (H + 63) / 64;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < all_chunks;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const bool gu = i < gu_chunks;
+    const int64_t j = gu ? i : i - gu_chunks;
+    const int64_t box = j / 1024;
+    const int r = (int)((j % 1024) / 8);
+    const int c = (int)(j % 8) ^ (r & 7);  // the chunk stored at this position
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (gu) {
+      const int64_t t = box / kb1, kb = box % kb1;
+      const int64_t unit = t * 64 + (r & 63);
+      const int64_t k = kb * 64 + c * 8;
+      if (unit < H && k < D)
+        v = *reinterpret_cast<const uint4*>(Wgu + ((r < 64 ? unit : H + unit) * D + k) * 2);
+    } else {
+      const int64_t t = box / kb2, kb = box % kb2;
+      const int64_t row = t * 128 + r;
+      const int64_t k = kb * 64 + c * 8;
+      if (row < D && k < H) v = *reinterpret_cast<const uint4*>(Wd + (row * H + k) * 2);
+    }
+    out[i] = v;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // no-grad forward for M <= 64 tokens: split-contraction swap-AB kernels
 // ---------------------------------------------------------------------------
 constexpr int NG_MAX_M = 64;
@@ -604,10 +653,10 @@ size_t ng_two_bytes(const NgPlan& p) {
   return WS_HEADER + p.counter_bytes + (slots1 > slots2 ? slots1 : slots2) * 128 * p.NT * 4;
 }
 
-template <int NT, bool GATE_UP, bool BF16>
+template <int NT, bool GATE_UP, bool BF16, bool PACKED = false>
 cudaError_t launch_ng(int kid, const CUtensorMap& tw, const CUtensorMap& tx, NgArgs a,
                       cudaStream_t st) {
-  auto kern = ng_gemm_kernel<NT, GATE_UP, BF16>;
+  auto kern = ng_gemm_kernel<NT, GATE_UP, BF16, PACKED>;
   constexpr int smem = NgSmem<NT>::DYN_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -640,30 +689,39 @@ cudaError_t launch_ng(int kid, const CUtensorMap& tw, const CUtensorMap& tx, NgA
 // must be zero when a call starts: each kernel zeroes the other's counters
 // at its start and every tile's reducer zeroes its own, so a zero-filled
 // workspace stays valid across calls.
+// With `packed` (swiglu_mlp_pack_weights' layout) the weight boxes come from
+// it by bulk copies and Wgu / Wd are not read.
 template <int NT, bool BF16>
 swiglu_status ng_forward_nt(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
                             int64_t M, int64_t D, int64_t H, const NgPlan& p, char* ws,
-                            size_t ws_cap, const Opts& o, cudaStream_t st) {
+                            size_t ws_cap, const Opts& o, cudaStream_t st,
+                            const uint8_t* packed = nullptr) {
   int* err = reinterpret_cast<int*>(ws);
   int* counters = reinterpret_cast<int*>(ws + WS_HEADER);
   float* part = reinterpret_cast<float*>(ws + WS_HEADER + p.counter_bytes);
   const uint64_t wl = g_wait_limit_ns.load();
-  CUtensorMap tw, tx;
-  if (!encode_gateup(&tw, BF16, Wgu, D, H, 64) || !map_kmajor(&tx, BF16, X, D, M, D, NT))
+  CUtensorMap tw = {}, tx;
+  if ((packed == nullptr && !encode_gateup(&tw, BF16, Wgu, D, H, 64)) ||
+      !map_kmajor(&tx, BF16, X, D, M, D, NT))
     return SWIGLU_ERR_CUDA;
   NgArgs a1{(int)M, (int)H, p.kb1, p.t1, 0, 0, part, counters, counters + p.t1, p.t2, 1, 0, 0,
             A, H, wl, err};
   a1.scale = o.gm;
+  a1.wpack = packed;
   set_windows(a1, {{A, (size_t)(M * H * 2)}, {ws, ws_cap}});
-  if (launch_ng<NT, true, BF16>(K_NG_GATE_UP, tw, tx, a1, st) != cudaSuccess)
+  if ((packed ? launch_ng<NT, true, BF16, true>(K_NG_GATE_UP, tw, tx, a1, st)
+              : launch_ng<NT, true, BF16>(K_NG_GATE_UP, tw, tx, a1, st)) != cudaSuccess)
     return SWIGLU_ERR_CUDA;
-  if (!map_kmajor(&tw, BF16, Wd, H, D, H, 128) || !map_kmajor(&tx, BF16, A, H, M, H, NT))
+  if ((packed == nullptr && !map_kmajor(&tw, BF16, Wd, H, D, H, 128)) ||
+      !map_kmajor(&tx, BF16, A, H, M, H, NT))
     return SWIGLU_ERR_CUDA;
   NgArgs a2{(int)M, (int)D, p.kb2, p.t2, 0, 0, part, counters + p.t1, counters, p.t1, 0, 1, 0,
             Y, D, wl, err};
   a2.scale = o.dm;
+  a2.wpack = packed ? packed + packed_gateup_bytes(D, H) : nullptr;
   set_windows(a2, {{Y, (size_t)(M * D * 2)}, {ws, ws_cap}});
-  return cuda_status(launch_ng<NT, false, BF16>(K_NG_DOWN, tw, tx, a2, st));
+  return cuda_status(packed ? launch_ng<NT, false, BF16, true>(K_NG_DOWN, tw, tx, a2, st)
+                            : launch_ng<NT, false, BF16>(K_NG_DOWN, tw, tx, a2, st));
 }
 
 constexpr size_t NG_DONE_OFFSET = 128;  // the fused kernel's finished-CTA count (header)
@@ -1167,6 +1225,67 @@ swiglu_status swiglu_mlp_fwd_nograd(const void* X, const void* Wgu, const void* 
                                     void* ws, size_t ws_bytes, void* stream) {
   return swiglu_mlp_fwd_nograd_ex(X, Wgu, Wd, Y, A, M, D, H, dtype, nullptr, ws, ws_bytes,
                                   stream);
+}
+
+size_t swiglu_mlp_packed_weights_bytes(int64_t D, int64_t H, swiglu_dtype dtype) {
+  if (D <= 0 || H <= 0 || (dtype != SWIGLU_BF16 && dtype != SWIGLU_F16)) return 0;
+  return packed_gateup_bytes(D, H) + packed_down_bytes(D, H);
+}
+
+swiglu_status swiglu_mlp_pack_weights(const void* Wgu, const void* Wd, void* packed, int64_t D,
+                                      int64_t H, swiglu_dtype dtype, void* stream) {
+  g_last_launches.store(0);
+  if (dtype != SWIGLU_BF16 && dtype != SWIGLU_F16) return SWIGLU_ERR_UNSUPPORTED;
+  if (D <= 0 || H <= 0) return SWIGLU_ERR_INVALID_ARG;
+  if (D % 8 != 0 || H % 8 != 0) return SWIGLU_ERR_ALIGNMENT;
+  if (D > 0x7fffffffLL || 3 * H > 0x7fffffffLL) return SWIGLU_ERR_UNSUPPORTED;
+  swiglu_status st = check_ptrs({Wgu, Wd, packed});
+  if (st != SWIGLU_OK) return st;
+  const int64_t gu_chunks = (int64_t)(packed_gateup_bytes(D, H) / 16);
+  const int64_t all = gu_chunks + (int64_t)(packed_down_bytes(D, H) / 16);
+  const int nsm = sm_count();
+  const int64_t want = (all + 255) / 256;
+  const int grid = (int)(want < (int64_t)(nsm > 0 ? nsm : 1) * 8 ? want : (int64_t)(nsm > 0 ? nsm : 1) * 8);
+  pack_weights_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint8_t*>(Wgu), static_cast<const uint8_t*>(Wd),
+      static_cast<uint4*>(packed), D, H, gu_chunks, all);
+  g_last_launches.fetch_add(1);
+  return cuda_status(cudaGetLastError());
+}
+
+swiglu_status swiglu_mlp_fwd_nograd_packed(const void* X, const void* packed, void* Y, void* A,
+                                           int64_t M, int64_t D, int64_t H, swiglu_dtype dtype,
+                                           const swiglu_mlp_options* options, void* ws,
+                                           size_t ws_bytes, void* stream) {
+  g_last_launches.store(0);
+  Opts o;
+  swiglu_status st = read_opts(options, false, &o);
+  if (st != SWIGLU_OK) return st;
+  if (dtype != SWIGLU_BF16 && dtype != SWIGLU_F16) return SWIGLU_ERR_UNSUPPORTED;
+  if (M > NG_MAX_M) return SWIGLU_ERR_UNSUPPORTED;
+  st = check_common(M, D, H, dtype, ws, ws_bytes, SWIGLU_OP_FWD_NOGRAD);
+  if (st != SWIGLU_OK) return st;
+  if (M == 0) return SWIGLU_OK;
+  if ((st = check_ptrs({X, packed, Y, A})) != SWIGLU_OK) return st;
+  const NgPlan p = ng_plan(M, D, H);
+  if (ng_two_bytes(p) > ws_bytes) return SWIGLU_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  switch (p.NT) {
+    case 16:
+      return dtype == SWIGLU_BF16
+                 ? ng_forward_nt<16, true>(X, nullptr, nullptr, Y, A, M, D, H, p, w, ws_bytes, o, s, pk)
+                 : ng_forward_nt<16, false>(X, nullptr, nullptr, Y, A, M, D, H, p, w, ws_bytes, o, s, pk);
+    case 32:
+      return dtype == SWIGLU_BF16
+                 ? ng_forward_nt<32, true>(X, nullptr, nullptr, Y, A, M, D, H, p, w, ws_bytes, o, s, pk)
+                 : ng_forward_nt<32, false>(X, nullptr, nullptr, Y, A, M, D, H, p, w, ws_bytes, o, s, pk);
+    default:
+      return dtype == SWIGLU_BF16
+                 ? ng_forward_nt<64, true>(X, nullptr, nullptr, Y, A, M, D, H, p, w, ws_bytes, o, s, pk)
+                 : ng_forward_nt<64, false>(X, nullptr, nullptr, Y, A, M, D, H, p, w, ws_bytes, o, s, pk);
+  }
 }
 
 swiglu_status swiglu_mlp_fwd_nograd_noalloc(const void* X, const void* Wgu, const void* Wd,

@@ -418,22 +418,54 @@ def _nograd_sweep(api, device, peaks, sizes=NOGRAD_S):
         tmed = statistics.median(times)
         byts = metrics.nograd_algorithmic_bytes(S, D, H)
         loop = _decode_loop(api, X, wts, o, ws)
+        packed = {}
+        if S <= NOGRAD_PACKED_MAX_S:
+            # the same call on the packed weight copy (same bytes, contiguous blocks)
+            pk = api.swiglu_mlp_pack_weights(wts["Wgu"], wts["Wd"])
+            call = lambda: api.swiglu_mlp_fwd_nograd_packed(X, pk, H, out=o, ws=ws)
+            for _ in range(10):
+                flush.sum()
+                call()
+            tp = []
+            for it in range(20):
+                flush.sum()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                call()
+                e1.record(st)
+                e1.synchronize()
+                tp.append(e0.elapsed_time(e1) / 1e3)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(DECODE_REPS):
+                call()
+            torch.cuda.synchronize()
+            lp = (time.perf_counter() - t0) / DECODE_REPS
+            tpm = statistics.median(tp)
+            packed = {"us_packed": round(tpm * 1e6, 2),
+                      "hbm_frac_packed": round(byts / tpm / 1e9 / peaks["hbm_gbs"], 4),
+                      "loop_us_packed": round(lp * 1e6, 2),
+                      "loop_hbm_frac_packed": round(byts / lp / 1e9 / peaks["hbm_gbs"], 4)}
+            del pk
         res.append({"S": S, "us": round(tmed * 1e6, 2), "GBps": round(byts / tmed / 1e9, 1),
                     "hbm_frac": round(byts / tmed / 1e9 / peaks["hbm_gbs"], 4),
                     "TFLOPS": round(metrics.fwd_flops(S, D, H) / tmed / 1e12, 2),
                     "kernel_us": kern, **loop,
                     # the same bytes per call in the back-to-back loop (host wall clock)
                     "loop_hbm_frac": round(byts / (loop["loop_us_direct"] * 1e-6) / 1e9
-                                           / peaks["hbm_gbs"], 4)})
+                                           / peaks["hbm_gbs"], 4), **packed})
     return {"workload": "B1_D4096_H11008_bf16_nograd", "l2": "flushed (512 MiB read) before "
             "each timed call", "median_of": 20,
             "decode_loop": "%d back-to-back calls, host wall clock per call (launch cost "
                            "included, no flush: the 270 MB of weights exceed L2): direct C-ABI "
                            "calls vs replays of the captured graph" % DECODE_REPS,
+            "packed": "*_packed: the same call on the weight copy written by "
+                      "swiglu_mlp_pack_weights (S <= %d)" % NOGRAD_PACKED_MAX_S,
             "sweep": res}
 
 
 DECODE_REPS = 200
+NOGRAD_PACKED_MAX_S = 64  # the packed-weights form serves the few-token path
 
 
 def _decode_loop(api, X, wts, o, ws):

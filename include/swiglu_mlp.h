@@ -244,6 +244,47 @@ swiglu_status swiglu_mlp_fwd_nograd_ex(const void* X, const void* Wgu, const voi
                                        void* A, int64_t M, int64_t D, int64_t H,
                                        swiglu_dtype dtype, const swiglu_mlp_options* options,
                                        void* ws, size_t ws_bytes, void* stream);
+
+/* Bytes of the packed copy of a layer's weights that
+ * swiglu_mlp_pack_weights writes: ceil(H/64) * ceil(D/64) + ceil(D/128) *
+ * ceil(H/64) blocks of 16 KB (about the size of Wgu and Wd together).  0 for
+ * invalid sizes or a dtype other than bf16/fp16. */
+size_t swiglu_mlp_packed_weights_bytes(int64_t D, int64_t H, swiglu_dtype dtype);
+
+/* Writes a packed copy of Wgu [2H,D] and Wd [D,H] (bf16 or fp16) to
+ * `packed` (device, 16-byte aligned, swiglu_mlp_packed_weights_bytes bytes)
+ * for swiglu_mlp_fwd_nograd_packed.  The few-token no-grad kernels stream
+ * each weight matrix as 16 KB blocks of 128 rows x 64 elements of K; the
+ * packed copy stores each block contiguously, in the order the kernels
+ * consume them and already in the 128-byte swizzled form they load into
+ * shared memory, so each CTA reads one contiguous range (measured on GB300:
+ * ~6.3 TB/s for contiguous 16 KB bulk copies against ~5.8 TB/s for the same
+ * bytes as 128-byte rows of the row-major matrices).  The pages have no
+ * counterpart: it is an inference-side layout option of this library.
+ * Layout: the gate/up blocks, then the down blocks.  Gate/up block (t, kb)
+ * at (t * ceil(D/64) + kb) * 16 KB: rows 0..63 are Wg rows t*64.., rows
+ * 64..127 the Wu rows of the same hidden units, elements kb*64.. of K; down
+ * block (t, kb) at gate/up bytes + (t * ceil(H/64) + kb) * 16 KB: Wd rows
+ * t*128.., elements kb*64.. of K.  Within a block, the 16-byte chunk c of row
+ * r is at r*128 + (c ^ (r mod 8))*16; elements past D or H are zero.  One
+ * kernel on `stream`; D and H multiples of 8.  Rewrite the copy whenever the
+ * weights change: the packed forward never reads Wgu or Wd. */
+swiglu_status swiglu_mlp_pack_weights(const void* Wgu, const void* Wd, void* packed, int64_t D,
+                                      int64_t H, swiglu_dtype dtype, void* stream);
+
+/* swiglu_mlp_fwd_nograd (with options as swiglu_mlp_fwd_nograd_ex: the gate
+ * and down multipliers) for 0 <= M <= 64 tokens, reading the weights from a
+ * copy written by swiglu_mlp_pack_weights instead of Wgu / Wd.  Runs the
+ * two-kernel few-token form; its outputs are bitwise equal to
+ * swiglu_mlp_fwd_nograd's two-kernel form on the same weights (the kernels
+ * see the same shared-memory contents).  M > 64 and fp32 return
+ * SWIGLU_ERR_UNSUPPORTED (keep the row-major weights for larger batches);
+ * the workspace is that of swiglu_mlp_fwd_nograd. */
+swiglu_status swiglu_mlp_fwd_nograd_packed(const void* X, const void* packed, void* Y, void* A,
+                                           int64_t M, int64_t D, int64_t H, swiglu_dtype dtype,
+                                           const swiglu_mlp_options* options, void* ws,
+                                           size_t ws_bytes, void* stream);
+
 swiglu_status swiglu_mlp_bwd_ex(const void* dY, const void* X, const void* Wgu, const void* Wd,
                                 void* saved, void* dX, void* dWgu, void* dWd, int64_t M,
                                 int64_t D, int64_t H, swiglu_dtype dtype,

@@ -53,6 +53,29 @@ def test_sizes(L):
     assert L.swiglu_mlp_saved_bytes(32, 176, 2) == 32 * 528 * 4
     for op in (0, 1, 2):
         assert L.swiglu_mlp_workspace_bytes(65536, 4096, 11008, 0, op) >= 4
+    # packed weights: 16 KB blocks, ceil(H/64) x ceil(D/64) for gate/up and
+    # ceil(D/128) x ceil(H/64) for down; bf16/fp16 only
+    assert L.swiglu_mlp_packed_weights_bytes(4096, 11008, 0) == (172 * 64 + 32 * 172) * 16384
+    assert L.swiglu_mlp_packed_weights_bytes(72, 80, 1) == (2 * 2 + 1 * 2) * 16384
+    assert L.swiglu_mlp_packed_weights_bytes(64, 64, 2) == 0
+    assert L.swiglu_mlp_packed_weights_bytes(0, 64, 0) == 0
+
+
+def test_packed_entry_points_check_arguments_first(L):
+    P = ctypes.c_void_p(256)
+    N = ctypes.c_void_p(0)
+    assert L.swiglu_mlp_pack_weights(P, P, P, 64, 128, 2, N) == UNSUP
+    assert L.swiglu_mlp_pack_weights(P, P, N, 64, 128, 0, N) == INVALID
+    assert L.swiglu_mlp_pack_weights(P, P, P, 60, 128, 0, N) == ALIGN
+    assert L.swiglu_mlp_pack_weights(P, P, ctypes.c_void_p(264), 64, 128, 0, N) == ALIGN
+    ws = ctypes.c_void_p(4096)
+    big = 1 << 30
+    assert L.swiglu_mlp_fwd_nograd_packed(P, P, P, P, 65, 64, 128, 0, N, ws, big, N) == UNSUP
+    assert L.swiglu_mlp_fwd_nograd_packed(P, P, P, P, 4, 64, 128, 2, N, ws, big, N) == UNSUP
+    assert L.swiglu_mlp_fwd_nograd_packed(P, N, P, P, 4, 64, 128, 0, N, ws, big, N) == INVALID
+    assert L.swiglu_mlp_fwd_nograd_packed(P, P, P, P, 4, 64, 128, 0, N, ws, 8, N) == WSERR
+    assert L.swiglu_mlp_fwd_nograd_packed(P, P, P, P, 0, 64, 128, 0, N, ws, big, N) == OK
+    assert L.swiglu_mlp_last_launch_count() == 0
 
 
 def test_status_strings(L):
