@@ -80,6 +80,39 @@ def test_no_grad_uses_inference_path():
     assert torch.equal(y, Yn)
 
 
+def test_packed_inference_copy_is_used_and_dropped_on_update():
+    """pack_for_inference: no-grad calls of up to 64 tokens stream the packed
+    copy (bitwise equal to the plain path, a single packed launch pair); an
+    in-place weight update drops the copy, so the next call reads the new
+    weights; calls with more tokens or with autograd take the usual paths."""
+    t = synthetic.make_inputs(16, 256, 392, "bf16", seed=29, device="cuda")
+    m = _module(t).pack_for_inference()
+    x = t["X"]
+    with torch.no_grad():
+        y = m(x)
+        y_ref, _ = api.swiglu_mlp_fwd_nograd(x, m.gate_up_weight, m.down_weight)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref)
+        assert m._packed_copy() is not None
+        m.down_weight.mul_(0.5)  # an optimiser-style in-place update
+        y2 = m(x)
+        assert m._packed_copy() is None
+        y2_ref, _ = api.swiglu_mlp_fwd_nograd(x, m.gate_up_weight, m.down_weight)
+        torch.cuda.synchronize()
+        assert torch.equal(y2, y2_ref) and not torch.equal(y2, y)
+        m.pack_for_inference()
+        x65 = torch.randn(65, 256, device="cuda").bfloat16()
+        y65 = m(x65)  # beyond the few-token path: the row-major weights
+        y65_ref, _ = api.swiglu_mlp_fwd_nograd(x65, m.gate_up_weight, m.down_weight)
+        torch.cuda.synchronize()
+        assert torch.equal(y65, y65_ref)
+    xg = x.clone().requires_grad_(True)
+    yg = m(xg)  # autograd: the training kernels, G/U saved
+    assert yg.grad_fn is not None
+    m.pack_for_inference(False)
+    assert m._packed_copy() is None
+
+
 def test_second_backward_is_refused():
     t = synthetic.make_inputs(64, 64, 176, "bf16", seed=24, device="cuda")
     m = _module(t)
