@@ -2,7 +2,7 @@
 // the work is bound by streaming the weights from HBM, not by the tensor core.
 //
 // Swap-AB: 128 weight rows take the MMA's M dimension and the (padded) tokens
-// its N dimension (NT = 16, 32 or 64), so one tcgen05.mma M=128 x N=NT x K=16
+// its N dimension (NT = 16, 32, 48 or 64), so one tcgen05.mma M=128 x N=NT x K=16
 // consumes 4 KB of weights.  The weight stream is spread evenly over every
 // SM by a stream-K decomposition: the tiles' k-blocks are laid end to end
 // (tile-major) and each persistent CTA (one per SM) takes one contiguous
@@ -100,7 +100,8 @@ struct NgSmem {
   static constexpr int MISC_OFFSET = BAR_OFFSET + NUM_BARS * 8;
   static constexpr int TOTAL = MISC_OFFSET + 16;
   static constexpr int DYN_BYTES = TOTAL + 1024;
-  static constexpr int TMEM_COLS = 2 * NT < 32 ? 32 : 2 * NT;
+  // two accumulators, allocated as a power of two of at least 32 columns
+  static constexpr int TMEM_COLS = 2 * NT <= 32 ? 32 : (2 * NT <= 64 ? 64 : (2 * NT <= 128 ? 128 : 256));
 };
 
 // Named barrier 1 over the 128 epilogue threads (warps 2..5).
@@ -382,7 +383,7 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
     ng_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const NgArgs a) {
   using L = NgSmem<NT>;
-  static_assert(NT == 16 || NT == 32 || NT == 64, "NT must be 16, 32 or 64");
+  static_assert(NT == 16 || NT == 32 || NT == 48 || NT == 64, "NT must be 16, 32, 48 or 64");
   static_assert(L::TOTAL + 1024 <= 232448, "shared memory plan exceeds 227 KB");
   constexpr int TILE_ROWS = GATE_UP ? 64 : 128;  // output rows (hidden units / features) per tile
 

@@ -551,9 +551,12 @@ bool ng_eligible(int64_t M, int64_t D, int64_t H, swiglu_dtype dt) {
 // ceil(range / kb) + 1 tiles, so ctas x seg_max <= tiles + 3 ctas partial
 // slots for any grid up to NG_MAX_CTAS: the workspace bound below does not
 // depend on the device.
-NgPlan ng_plan(int64_t M, int64_t D, int64_t H) {
+// The token block: the smallest of 16, 32, 48, 64 that holds M (the two
+// kernels' time tracks the token rows landed per weight box, padding rows
+// included); the fused kernel takes 16, 32 or 64 (ng_fused_plan).
+NgPlan ng_plan(int64_t M, int64_t D, int64_t H, int nt = 0) {
   NgPlan p;
-  p.NT = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+  p.NT = nt > 0 ? nt : (M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 48 ? 48 : 64)));
   p.t1 = (int)((H + 63) / 64);
   p.kb1 = (int)((D + 63) / 64);
   p.t2 = (int)((D + 127) / 128);
@@ -563,6 +566,10 @@ NgPlan ng_plan(int64_t M, int64_t D, int64_t H) {
   const size_t slots = (size_t)(p.t1 > p.t2 ? p.t1 : p.t2) + 3 * NG_MAX_CTAS;
   p.part_bytes = slots * 128 * p.NT * 4;
   return p;
+}
+
+NgPlan ng_fused_plan(int64_t M, int64_t D, int64_t H) {
+  return ng_plan(M, D, H, M <= 16 ? 16 : (M <= 32 ? 32 : 64));
 }
 
 // CTAs, stream-K tiles and partial slots per CTA of one GEMM over at most
@@ -790,16 +797,24 @@ swiglu_status ng_forward_fused(const void* X, const void* Wgu, const void* Wd, v
   return cuda_status(cudaGetLastError());
 }
 
-// The fused form when it is selected (by default for 33..64 tokens, where
-// it measured faster; for fewer tokens both forms take the same time) and,
-// for a fixed scratch array, its workspace fits `ws_cap`; else two kernels.
+// The fused form when it is selected (swiglu_mlp_set_nograd_fused: never by
+// default, for 33..64 tokens, or always) and its workspace fits `ws_cap` (a
+// fixed scratch array may not hold it); else two kernels.
 template <int NT, bool BF16>
 swiglu_status ng_forward_t(const void* X, const void* Wgu, const void* Wd, void* Y, void* A,
                            int64_t M, int64_t D, int64_t H, const NgPlan& p, char* ws,
                            size_t ws_cap, const Opts& o, cudaStream_t st) {
   const int mode = g_ng_fused.load();
-  if ((mode == 2 || (mode == 1 && NT == 64)) && ng_fused_bytes(p) <= ws_cap)
-    return ng_forward_fused<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, o, st);
+  if (mode == 2 || (mode == 1 && M > 32)) {
+    const NgPlan pf = ng_fused_plan(M, D, H);
+    if (ng_fused_bytes(pf) <= ws_cap) {
+      switch (pf.NT) {
+        case 16: return ng_forward_fused<16, BF16>(X, Wgu, Wd, Y, A, M, D, H, pf, ws, ws_cap, o, st);
+        case 32: return ng_forward_fused<32, BF16>(X, Wgu, Wd, Y, A, M, D, H, pf, ws, ws_cap, o, st);
+        default: return ng_forward_fused<64, BF16>(X, Wgu, Wd, Y, A, M, D, H, pf, ws, ws_cap, o, st);
+      }
+    }
+  }
   if (ng_two_bytes(p) > ws_cap) return SWIGLU_ERR_UNSUPPORTED;
   return ng_forward_nt<NT, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, o, st);
 }
@@ -812,6 +827,7 @@ swiglu_status ng_forward(const void* X, const void* Wgu, const void* Wd, void* Y
   switch (p.NT) {
     case 16: return ng_forward_t<16, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, o, st);
     case 32: return ng_forward_t<32, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, o, st);
+    case 48: return ng_forward_t<48, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, o, st);
     default: return ng_forward_t<64, BF16>(X, Wgu, Wd, Y, A, M, D, H, p, ws, ws_cap, o, st);
   }
 }
@@ -1135,7 +1151,7 @@ size_t swiglu_mlp_workspace_bytes(int64_t M, int64_t D, int64_t H, swiglu_dtype 
   if (op == SWIGLU_OP_FWD_NOGRAD && D > 0 && H > 0 && ng_eligible(M, D, H, dtype)) {
     const NgPlan p = ng_plan(M, D, H);
     const size_t two = WS_HEADER + p.counter_bytes + p.part_bytes;
-    const size_t one = ng_fused_bytes(p);
+    const size_t one = ng_fused_bytes(ng_fused_plan(M, D, H));
     return two > one ? two : one;
   }
   if (dtype == SWIGLU_BF16 || dtype == SWIGLU_F16)
@@ -1281,6 +1297,10 @@ swiglu_status swiglu_mlp_fwd_nograd_packed(const void* X, const void* packed, vo
       return dtype == SWIGLU_BF16
                  ? ng_forward_nt<32, true>(X, nullptr, nullptr, Y, A, M, D, H, p, w, ws_bytes, o, s, pk)
                  : ng_forward_nt<32, false>(X, nullptr, nullptr, Y, A, M, D, H, p, w, ws_bytes, o, s, pk);
+    case 48:
+      return dtype == SWIGLU_BF16
+                 ? ng_forward_nt<48, true>(X, nullptr, nullptr, Y, A, M, D, H, p, w, ws_bytes, o, s, pk)
+                 : ng_forward_nt<48, false>(X, nullptr, nullptr, Y, A, M, D, H, p, w, ws_bytes, o, s, pk);
     default:
       return dtype == SWIGLU_BF16
                  ? ng_forward_nt<64, true>(X, nullptr, nullptr, Y, A, M, D, H, p, w, ws_bytes, o, s, pk)
@@ -1302,7 +1322,8 @@ swiglu_status swiglu_mlp_fwd_nograd_noalloc(const void* X, const void* Wgu, cons
   void* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != SWIGLU_OK) return st;
   const NgPlan p = ng_plan(M, D, H);
-  if (ng_two_bytes(p) > NOALLOC_SCRATCH_BYTES && ng_fused_bytes(p) > NOALLOC_SCRATCH_BYTES)
+  if (ng_two_bytes(p) > NOALLOC_SCRATCH_BYTES &&
+      ng_fused_bytes(ng_fused_plan(M, D, H)) > NOALLOC_SCRATCH_BYTES)
     return SWIGLU_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: clear the error word, the

@@ -88,9 +88,10 @@ def test_packed_layout_matches_its_definition(D, H):
 
 @pytest.mark.parametrize("dtn", ["bf16", "f16"])
 @pytest.mark.parametrize("M,D,H", [(1, 320, 392), (5, 320, 392), (16, 320, 392), (17, 320, 392),
-                                   (33, 320, 392), (64, 320, 392), (3, 72, 80),
+                                   (33, 320, 392), (40, 320, 392), (48, 320, 392),
+                                   (64, 320, 392), (3, 72, 80),
                                    (1, 4096, 11008), (16, 4096, 11008), (32, 4096, 11008),
-                                   (64, 4096, 11008)])
+                                   (48, 4096, 11008), (64, 4096, 11008)])
 def test_packed_forward_bitwise_equals_plain(M, D, H, dtn):
     t = synthetic.make_inputs(M, D, H, dtn, seed=500 + M, device="cuda", kind="device")
     packed = api.swiglu_mlp_pack_weights(t["Wgu"], t["Wd"])

@@ -368,7 +368,7 @@ def ng_mode(request):
 
 
 @pytest.mark.parametrize("dtn", ["bf16", "f16"])
-@pytest.mark.parametrize("M", [1, 5, 16, 17, 33, 64, 65, 100, 128])
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 33, 40, 48, 49, 64, 65, 100, 128])
 def test_nograd_small_m_parity(M, dtn, ng_mode):
     """Few-token no-grad path (split contraction, per-tile reduction): ragged
     hidden and feature tiles, several splits per tile, against the oracle and

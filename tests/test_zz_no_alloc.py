@@ -48,7 +48,8 @@ def _noalloc(L, t, M, D, H, dt):
 
 @pytest.mark.parametrize("dtn,M,D,H", [("bf16", 1, 4096, 11008), ("bf16", 16, 4096, 11008),
                                        ("bf16", 32, 4096, 11008), ("f16", 5, 320, 392),
-                                       ("bf16", 32, 512, 1024), ("bf16", 64, 4096, 11008)])
+                                       ("bf16", 32, 512, 1024), ("bf16", 40, 4096, 11008),
+                                       ("bf16", 64, 4096, 11008)])
 def test_noalloc_matches_workspace_entry_point(L, dtn, M, D, H):
     # the default few-token form (two kernels) at 1 to 64 tokens
     dt = {"bf16": 0, "f16": 1}[dtn]
