@@ -104,6 +104,16 @@ struct NgSmem {
   static constexpr int TMEM_COLS = 2 * NT <= 32 ? 32 : (2 * NT <= 64 ? 64 : (2 * NT <= 128 ? 128 : 256));
 };
 
+// Token rows the two-kernel form loads per k-block: M rounded up to the
+// 8-row swizzle atom, at most NT.  The MMA still reads NT rows; rows past
+// these hold whatever the ring slot held before, and only feed accumulator
+// columns of tokens >= M, which no epilogue stores (a column depends on its
+// own token row alone), so the stored outputs are the same bits.
+__host__ __device__ inline int ng_x_rows(int NT, int M) {
+  const int r = (M + 7) & ~7;
+  return r < NT ? r : NT;
+}
+
 // Named barrier 1 over the 128 epilogue threads (warps 2..5).
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -458,6 +468,9 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
       tma_load_2d(slot, &tmW, bar, kb * TC_BK, tile * TILE_ROWS);
   };
 
+  // bytes per ring slot: the weight box and the token rows actually loaded
+  const uint32_t stage_tx = L::W_BYTES + (uint32_t)ng_x_rows(NT, a.M) * 128u;
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -477,7 +490,7 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
           for (int i = 0; i < nkb && pending_x < L::STAGES; ++i) {
             const int k0 = (kb0 + i) * TC_BK;
             const uint32_t sw = sbase + pending_x * L::STAGE_BYTES;
-            mbar_arrive_expect_tx(full_bar(pending_x), L::STAGE_BYTES);
+            mbar_arrive_expect_tx(full_bar(pending_x), stage_tx);
             load_w(sw, full_bar(pending_x), tile, kb0 + i);
             pending_k0[pending_x] = k0;
             issued_mask |= 1u << pending_x;
@@ -512,7 +525,7 @@ __global__ void __launch_bounds__(NG_THREADS, 1)
           const uint32_t sw = sbase + stage * L::STAGE_BYTES;
           const uint32_t sx = sw + L::W_BYTES;
           const int k0 = (kb0 + i) * TC_BK;
-          mbar_arrive_expect_tx(full_bar(stage), L::STAGE_BYTES);
+          mbar_arrive_expect_tx(full_bar(stage), stage_tx);
           load_w(sw, full_bar(stage), tile, kb0 + i);
           tma_load_2d(sx, &tmX, full_bar(stage), k0, 0);
           issued_mask |= 1u << stage;

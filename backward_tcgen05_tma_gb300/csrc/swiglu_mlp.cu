@@ -709,7 +709,7 @@ swiglu_status ng_forward_nt(const void* X, const void* Wgu, const void* Wd, void
   const uint64_t wl = g_wait_limit_ns.load();
   CUtensorMap tw = {}, tx;
   if ((packed == nullptr && !encode_gateup(&tw, BF16, Wgu, D, H, 64)) ||
-      !map_kmajor(&tx, BF16, X, D, M, D, NT))
+      !map_kmajor(&tx, BF16, X, D, M, D, ng_x_rows(NT, (int)M)))
     return SWIGLU_ERR_CUDA;
   NgArgs a1{(int)M, (int)H, p.kb1, p.t1, 0, 0, part, counters, counters + p.t1, p.t2, 1, 0, 0,
             A, H, wl, err};
@@ -720,7 +720,7 @@ swiglu_status ng_forward_nt(const void* X, const void* Wgu, const void* Wd, void
               : launch_ng<NT, true, BF16>(K_NG_GATE_UP, tw, tx, a1, st)) != cudaSuccess)
     return SWIGLU_ERR_CUDA;
   if ((packed == nullptr && !map_kmajor(&tw, BF16, Wd, H, D, H, 128)) ||
-      !map_kmajor(&tx, BF16, A, H, M, H, NT))
+      !map_kmajor(&tx, BF16, A, H, M, H, ng_x_rows(NT, (int)M)))
     return SWIGLU_ERR_CUDA;
   NgArgs a2{(int)M, (int)D, p.kb2, p.t2, 0, 0, part, counters + p.t1, counters, p.t1, 0, 1, 0,
             Y, D, wl, err};
