@@ -44,7 +44,7 @@ MAIN = "B8_S8192_D4096_H11008"
 # the pages' own number for this workload: 1049.66 ms on an RTX 5060 Ti
 # (SM120), i.e. 18 M D H / t = 50.67 TFLOPS ("Training results" table)
 PAGES_TFLOPS = {MAIN: 18.0 * 65536 * 4096 * 11008 / 1.04966 / 1e12}
-NOGRAD_S = [1, 2, 4, 8, 16, 32, 64, 128, 256]
+NOGRAD_S = [1, 2, 4, 8, 16, 32, 48, 64, 128, 256]
 CPU_SAMPLE_TOKENS = 256
 REF_STEP_TOKENS = 8
 

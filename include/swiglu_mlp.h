@@ -355,8 +355,9 @@ int swiglu_mlp_set_cta_pairs(int mode);
  * ready mask in the workspace); or as two kernels (gate/up, then the down
  * projection as a programmatic dependent launch).  mode 0 (the default):
  * always two kernels, measured faster at every size from 1 to 64 tokens
- * (62-63 vs 65-68 us at 1-16 tokens, 82-83 vs 87-89 us at 33-64, D = 4096,
- * H = 11008); 1: the fused kernel for 33..64 tokens, two kernels below; 2:
+ * (62-63 vs 65-68 us at 1-16 tokens, 72-83 vs 87-89 us at 33-64, D = 4096,
+ * H = 11008; the two kernels also take a 48-token block, the fused kernel
+ * 16, 32 or 64); 1: the fused kernel for 33..64 tokens, two kernels below; 2:
  * always the fused kernel.  Both forms are
  * deterministic (partial sums are added in a fixed order); they split the
  * contractions at different points, so their results differ in rounding
