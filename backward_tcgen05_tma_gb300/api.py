@@ -151,6 +151,8 @@ def _load(path: str) -> ctypes.CDLL:
     L.swiglu_mlp_set_cta_pairs.argtypes = [ci]
     L.swiglu_mlp_set_nograd_fused.restype = ci
     L.swiglu_mlp_set_nograd_fused.argtypes = [ci]
+    L.swiglu_mlp_set_wide_tiles.restype = ci
+    L.swiglu_mlp_set_wide_tiles.argtypes = [ci]
     L.swiglu_mlp_profile_enable.restype = None
     L.swiglu_mlp_profile_enable.argtypes = [ci]
     L.swiglu_mlp_profile_read.restype = ci
@@ -430,6 +432,13 @@ def swiglu_mlp_set_cta_pairs(mode: int = 1) -> int:
     """Tensor-core GEMMs on SM pairs: 1 = by size (default), 2 = always,
     0 = never; returns the previous mode."""
     return int(lib().swiglu_mlp_set_cta_pairs(int(mode)))
+
+
+def swiglu_mlp_set_wide_tiles(mode: int = 1) -> int:
+    """Weight-gradient and dX GEMMs on SM pairs: 1 = 512-column tiles by
+    size (the default), 0 = 256-column tiles, 2 = 512-column tiles always;
+    returns the previous mode."""
+    return int(lib().swiglu_mlp_set_wide_tiles(int(mode)))
 
 
 def swiglu_mlp_set_nograd_fused(mode: int = 0) -> int:

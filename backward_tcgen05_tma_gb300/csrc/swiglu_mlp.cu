@@ -105,6 +105,7 @@ bool take_inject() {
 }
 std::atomic<int> g_last_launches{0};
 std::atomic<int> g_cta_pairs{1};  // SM pairs (cta_group::2): 0 never, 1 by size, 2 always
+std::atomic<int> g_wide_tiles{1};  // 512-column pair tiles for dWd, dWgu, dX: 0 never, 1 by size, 2 always
 std::atomic<int> g_ng_fused{0};   // few-token no-grad: fused kernel 0 never, 1 for 33..64 tokens, 2 always
 constexpr int TC2_STAGES = 6;
 
@@ -278,9 +279,13 @@ size_t part_capacity(size_t ws_bytes) {
   return ws_bytes > fixed ? ws_bytes - fixed : 0;
 }
 
-size_t tc_part_bytes(const TcPlan& p) {
-  return p.sk_tiles ? (size_t)p.grid * p.seg_max * TC_BM * TC_BN * 4 : 0;
+size_t tc_part_bytes(const TcPlan& p, int64_t bn = TC_BN) {
+  return p.sk_tiles ? (size_t)p.grid * p.seg_max * TC_BM * bn * 4 : 0;
 }
+
+// 512-column pair tiles for the weight-gradient and dX GEMMs (use_wide)
+constexpr int TC2_WIDE_BN = 512;
+constexpr int64_t TC2_WIDE_MIN_K = 16384;
 
 int tc_nsm() {
   const int n = sm_count();
@@ -322,6 +327,21 @@ int tc2_units() {
   return cached[dev];
 }
 
+// 512-column pair tiles (one accumulator, no epilogue overlap) for an
+// M x N GEMM over K: by size, where the main loop dwarfs a tile's epilogue
+// (K >= 16384) and every pair gets at least two whole tiles.  Measured at
+// B=8 S=8192 D=4096 H=11008: dWd 3.74 -> 3.61, dWgu 7.46 -> 6.96, dX 7.17
+// -> 6.88 ms; at S=4096 D=2048 H=5632 dWgu 0.975 -> 0.897 ms, while dX
+// (K = 11264) and dWd (88 tiles for 76 pairs) were slower, which the rule
+// leaves on 256-column tiles.
+bool use_wide(bool pairs, int64_t M, int64_t N, int64_t K) {
+  const int mode = g_wide_tiles.load();
+  if (!pairs || mode == 0) return false;
+  if (mode == 2) return true;
+  const int64_t tiles = ((M + TC2_BM - 1) / TC2_BM) * ((N + TC2_WIDE_BN - 1) / TC2_WIDE_BN);
+  return K >= TC2_WIDE_MIN_K && tiles >= 2 * (int64_t)tc2_units();
+}
+
 // Whether one GEMM runs on SM pairs.  Measured per kernel on GB300: pairs
 // win when the main loop dominates -- long K and several rounds of tiles, or
 // the very long K of the weight gradients -- while short-K GEMMs with heavy
@@ -349,7 +369,7 @@ bool use_pairs(int64_t Mg, int64_t N, int64_t n_per_tile, int64_t K) {
 // (GEMM rows, GEMM columns, columns per tile, K).  Without a device the bound
 // for any GPU of up to 256 SMs (two slots per CTA).
 size_t tc_ws_part_bytes(int64_t M, int64_t D, int64_t H, int op) {
-  if (sm_count() < 1) return (size_t)2 * TC_SK_MAX_SMS * TC_BM * TC_BN * 4;
+  if (sm_count() < 1) return (size_t)2 * TC_SK_MAX_SMS * TC_BM * TC2_WIDE_BN * 4;
   const int nsm = tc_nsm();
   const int64_t fwd[2][4] = {{M, H, TC_BN / 2, D}, {M, D, TC_BN, H}};
   const int64_t bwd[4][4] = {{D, H, TC_BN, M}, {M, H, TC_BN, D}, {2 * H, D, TC_BN, M},
@@ -366,6 +386,13 @@ size_t tc_ws_part_bytes(int64_t M, int64_t D, int64_t H, int op) {
         units >= 1 ? 2 * tc_part_bytes(tc_plan(((g[0] + TC2_BM - 1) / TC2_BM) * nt, kb, units)) : 0;
     if (b1 > best) best = b1;
     if (b2 > best) best = b2;
+    if (op == SWIGLU_OP_BWD && units >= 1 && i != 1) {
+      // the same GEMM on 512-column pair tiles (dWd, dWgu, dX)
+      const int64_t ntw = (g[1] + TC2_WIDE_BN - 1) / TC2_WIDE_BN;
+      const size_t bw = 2 * tc_part_bytes(tc_plan(((g[0] + TC2_BM - 1) / TC2_BM) * ntw, kb, units),
+                                          TC2_WIDE_BN);
+      if (bw > best) best = bw;
+    }
   }
   return best;
 }
@@ -392,7 +419,7 @@ TcShape make_shape(int64_t M, int64_t N, int64_t K, int64_t n_per_tile, int* err
                            pairs ? tc2_units() : tc_nsm());
   s.sk_tiles = p.sk_tiles;
   s.seg_max = p.seg_max;
-  if (tc_part_bytes(p) * (pairs ? 2 : 1) > part_cap) {
+  if (tc_part_bytes(p, n_per_tile) * (pairs ? 2 : 1) > part_cap) {
     s.sk_tiles = 0;
     s.seg_max = 1;
   }
@@ -429,16 +456,17 @@ cudaError_t launch_tc(int kid, const CUtensorMap& ta, const CUtensorMap& tb, con
 
 // The pair kernel: clusters of two CTAs on the two SMs of a TPC.
 // tg, tu: the TMA dG/dU epilogue's maps of G and U (other epilogues: unused)
-template <int AM, int BMODE, bool BF16, class Epi>
+template <int AM, int BMODE, bool BF16, class Epi, int BN = TC2_BN>
 cudaError_t launch_tc2(int kid, const CUtensorMap& ta, const CUtensorMap& tb, const TcShape& s,
                        const typename Epi::Params& ep, cudaStream_t st,
                        const CUtensorMap* tg = nullptr, const CUtensorMap* tu = nullptr) {
   // the TMA dG/dU epilogue's slots (GU_SLOTS x 4 KB per epilogue warp) take
-  // the room of GU_SLOTS - 1 ring stages
+  // the room of GU_SLOTS - 1 ring stages; 512-column tiles (48 KB stages)
+  // keep four
   constexpr bool gu = epi_tma_gu<Epi>::value;
-  constexpr int stages = gu ? TC2_STAGES + 1 - GU_SLOTS : TC2_STAGES;
-  auto kern = tc2_gemm_kernel<stages, AM, BMODE, BF16, Epi>;
-  constexpr int smem = Tc2Smem<stages, gu>::DYN_BYTES;
+  constexpr int stages = BN > 256 ? 4 : (gu ? TC2_STAGES + 1 - GU_SLOTS : TC2_STAGES);
+  auto kern = tc2_gemm_kernel<stages, AM, BMODE, BF16, Epi, BN>;
+  constexpr int smem = Tc2Smem<stages, gu, BN>::DYN_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int units = launch_units(s, tc2_units());
@@ -971,10 +999,14 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     return SWIGLU_ERR_CUDA;
   {
     const bool pairs = use_pairs(D, H, TC_BN, M);
-    TcShape s = make_shape(D, H, M, TC_BN, err, pairs, cap);
+    const bool wide = use_wide(pairs, D, H, M);
+    TcShape s = make_shape(D, H, M, wide ? TC2_WIDE_BN : TC_BN, err, pairs, cap);
     set_windows(s, {{dWd, (size_t)(D * H * 2)}, {err, ws_bytes}});
     EpiStore::Params p{dWd, H, o.dm, o.acc};
-    e = launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWD, m1, m2, s, p, st);
+    e = wide ? launch_tc2<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore, TC2_WIDE_BN>(K_DWD, m1, m2,
+                                                                                 s, p, st)
+             : launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWD, m1, m2, s, p,
+                                                                      st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   // dA = dY Wd (Wd read MN-major as [K = D][N = H]); dG, dU written over G, U
@@ -1008,10 +1040,14 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     return SWIGLU_ERR_CUDA;
   {
     const bool pairs = use_pairs(2 * H, D, TC_BN, M);
-    TcShape s = make_shape(2 * H, D, M, TC_BN, err, pairs, cap);
+    const bool wide = use_wide(pairs, 2 * H, D, M);
+    TcShape s = make_shape(2 * H, D, M, wide ? TC2_WIDE_BN : TC_BN, err, pairs, cap);
     set_windows(s, {{dWgu, (size_t)(2 * H * D * 2)}, {err, ws_bytes}});
     EpiStore::Params p{dWgu, D, 1.0f, o.acc};
-    e = launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWGU, m1, m2, s, p, st);
+    e = wide ? launch_tc2<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore, TC2_WIDE_BN>(K_DWGU, m1, m2,
+                                                                                 s, p, st)
+             : launch_gemm<LOAD_MNMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DWGU, m1, m2, s,
+                                                                      p, st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   // dX [M, D] = [dG | dU] [Wg; Wu]: K = 2H in one accumulator
@@ -1019,10 +1055,14 @@ swiglu_status tc_backward(const void* dY, const void* X, const void* Wgu, const 
     return SWIGLU_ERR_CUDA;
   {
     const bool pairs = use_pairs(M, D, TC_BN, 2 * H);
-    TcShape s = make_shape(M, D, 2 * H, TC_BN, err, pairs, cap);
+    const bool wide = use_wide(pairs, M, D, 2 * H);
+    TcShape s = make_shape(M, D, 2 * H, wide ? TC2_WIDE_BN : TC_BN, err, pairs, cap);
     set_windows(s, {{dX, (size_t)(M * D * 2)}, {err, ws_bytes}});
     EpiStore::Params p{dX, D, 1.0f, 0};
-    e = launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DX, m1, m2, s, p, st);
+    e = wide ? launch_tc2<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore, TC2_WIDE_BN>(K_DX, m1, m2, s,
+                                                                                p, st)
+             : launch_gemm<LOAD_KMAJOR, LOAD_MNMAJOR, BF16, EpiStore>(pairs, K_DX, m1, m2, s, p,
+                                                                     st);
     if (e != cudaSuccess) return SWIGLU_ERR_CUDA;
   }
   return SWIGLU_OK;
@@ -1500,6 +1540,10 @@ int swiglu_mlp_set_nograd_fused(int mode) {
 
 int swiglu_mlp_set_cta_pairs(int mode) {
   return g_cta_pairs.exchange(mode <= 0 ? 0 : (mode >= 2 ? 2 : 1));
+}
+
+int swiglu_mlp_set_wide_tiles(int mode) {
+  return g_wide_tiles.exchange(mode <= 0 ? 0 : (mode >= 2 ? 2 : 1));
 }
 
 void swiglu_mlp_profile_enable(int on) { g_prof_on.store(on ? 1 : 0); }

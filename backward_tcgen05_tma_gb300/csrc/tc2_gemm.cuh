@@ -39,10 +39,15 @@ constexpr int GU_CHUNKS = TC2_BN / 64;  // 32-column chunks per warp and tile
 
 // GU: the epilogue is the TMA dG/dU form (G/U slots and their barriers
 // instead of the 2 KB store-staging buffers).
-template <int STAGES, bool GU = false>
+// BN: tile columns, 256 (two 256-column accumulators, the epilogue of one
+// tile overlapping the next tile's main loop) or 512 (one accumulator of all
+// 512 TMEM columns: each A k-block feeds twice the columns, for the long
+// contractions whose main loop dwarfs the epilogue).  Each CTA holds BN / 2
+// columns of B per stage, as BN / 256 chunks of 128.
+template <int STAGES, bool GU = false, int BN = TC2_BN>
 struct Tc2Smem {
-  static constexpr int A_BYTES = 128 * TC_BK * 2;  // this CTA's 128 rows of A
-  static constexpr int B_BYTES = 128 * TC_BK * 2;  // this CTA's 128 columns of B
+  static constexpr int A_BYTES = 128 * TC_BK * 2;       // this CTA's 128 rows of A
+  static constexpr int B_BYTES = (BN / 2) * TC_BK * 2;  // this CTA's BN / 2 columns of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;  // 8 warps x 2 KB store staging
   static constexpr int GU_OFFSET = EPI_OFFSET + (GU ? 0 : 8 * 2048);  // 8 warps x GU_SLOTS slots
@@ -54,7 +59,8 @@ struct Tc2Smem {
   static constexpr int MISC_OFFSET = BAR_OFFSET + NUM_BARS * 8;  // tmem slot, abort, last
   static constexpr int TOTAL = MISC_OFFSET + 16;
   static constexpr int DYN_BYTES = TOTAL + 1024;
-  static constexpr int TMEM_COLS = 2 * TC2_BN;
+  static constexpr int NACC = BN > 256 ? 1 : 2;  // accumulators in TMEM
+  static constexpr int TMEM_COLS = NACC * BN;
 };
 
 // Backward SwiGLU epilogue (the math of EpiDSwiGLUT) with its G/U traffic on
@@ -205,15 +211,19 @@ __device__ __forceinline__ bool dgu_tma_tile(GuPipe& gp, const CUtensorMap* gm,
   return true;
 }
 
-template <int STAGES, int A_MODE, int B_MODE, bool BF16, class Epi>
+template <int STAGES, int A_MODE, int B_MODE, bool BF16, class Epi, int BN = TC2_BN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const TcShape s,
                     const typename Epi::Params ep, const __grid_constant__ CUtensorMap tmG,
                     const __grid_constant__ CUtensorMap tmU) {
   constexpr bool TMA_GU = epi_tma_gu<Epi>::value;
-  using L = Tc2Smem<STAGES, TMA_GU>;
-  constexpr int BN = TC2_BN;
+  using L = Tc2Smem<STAGES, TMA_GU, BN>;
+  static_assert(BN == 256 || (BN == 512 && !TMA_GU && B_MODE != LOAD_GATEUP),
+                "512-column tiles serve the plain-store GEMMs");
+  constexpr int NACC = L::NACC;
+  constexpr int MMA_N = BN > 256 ? 256 : BN;  // columns per tcgen05.mma
+  constexpr int NCH = BN / 256;               // B chunks (of 128 columns per CTA) per stage
   static_assert(L::TOTAL + 1024 <= 232448, "shared memory plan exceeds 227 KB");
 
   extern __shared__ uint8_t smem_raw[];
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(full_bar(i), 1);
       mbar_init(empty_bar(i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 2; ++i) {  // (the second pair is unused with one accumulator)
       mbar_init(accf_bar(i), 1);
       mbar_init(acce_bar(i), 16);  // one arrival per epilogue warp of both CTAs
     }
@@ -288,7 +298,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         int mt, nt;
         tc_tile_coords(tile, s, mt, nt);
         const int m0 = mt * TC2_BM + (int)rank * 128;  // this CTA's rows of A
-        const int nb = nt * BN + (int)rank * 128;      // this CTA's columns of B
+        // this CTA's columns of B: in chunk j, nt * BN + j * 256 + rank * 128
+        const int nb = nt * BN + (int)rank * 128;
         for (int kb = kb0; kb < kb0 + nkb; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s.wait_limit_ns, abort_flag, s.err)) {
             ok = false;
@@ -308,14 +319,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               tma_load_2d_cg2(sa, &tmA, fb, m0, k0);
               tma_load_2d_cg2(sa + 8192, &tmA, fb, m0 + 64, k0);
             }
-            if (B_MODE == LOAD_KMAJOR) {
-              tma_load_2d_cg2(sb, &tmB, fb, k0, nb);
-            } else if (B_MODE == LOAD_GATEUP) {
+            if (B_MODE == LOAD_GATEUP) {
               // the even CTA brings the Wg rows, the odd one the Wu rows
               tma_load_3d_cg2(sb, &tmB, fb, k0, nt * (BN / 2), (int)rank);
             } else {
-              tma_load_2d_cg2(sb, &tmB, fb, nb, k0);
-              tma_load_2d_cg2(sb + 8192, &tmB, fb, nb + 64, k0);
+#pragma unroll
+              for (int j = 0; j < NCH; ++j) {
+                const uint32_t sbj = sb + j * 16384;
+                if (B_MODE == LOAD_KMAJOR) {
+                  tma_load_2d_cg2(sbj, &tmB, fb, k0, nb + j * 256);
+                } else {
+                  tma_load_2d_cg2(sbj, &tmB, fb, nb + j * 256, k0);
+                  tma_load_2d_cg2(sbj + 8192, &tmB, fb, nb + j * 256 + 64, k0);
+                }
+              }
             }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -338,7 +355,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       constexpr uint32_t idesc =
-          make_idesc_f16(BF16, A_MODE == LOAD_MNMAJOR, B_MODE == LOAD_MNMAJOR, TC2_BM, BN);
+          make_idesc_f16(BF16, A_MODE == LOAD_MNMAJOR, B_MODE == LOAD_MNMAJOR, TC2_BM, MMA_N);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -367,10 +384,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint64_t ad = (A_MODE == LOAD_MNMAJOR)
                                     ? make_sw128_desc(sa + kk * 2048, 8192, 1024)
                                     : make_sw128_desc(sa + kk * 32, 16, 1024);
-            const uint64_t bd = (B_MODE == LOAD_MNMAJOR)
-                                    ? make_sw128_desc(sb + kk * 2048, 8192, 1024)
-                                    : make_sw128_desc(sb + kk * 32, 16, 1024);
-            umma_f16_ss_cg2(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {  // chunk j: accumulator columns j*256..
+              const uint32_t sbj = sb + j * 16384;
+              const uint64_t bd = (B_MODE == LOAD_MNMAJOR)
+                                      ? make_sw128_desc(sbj + kk * 2048, 8192, 1024)
+                                      : make_sw128_desc(sbj + kk * 32, 16, 1024);
+              umma_f16_ss_cg2(d_tmem + j * MMA_N, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit_cg2_mc(empty_bar(stage), 0x3);  // frees the slot in both CTAs
           if (++stage == STAGES) {
@@ -380,7 +401,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         if (!ok) break;
         umma_commit_cg2_mc(accf_bar(acc), 0x3);  // accumulator complete in both CTAs
-        if (++acc == 2) {
+        if (++acc == NACC) {
           acc = 0;
           acc_phase ^= 1u;
         }
@@ -526,7 +547,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
-      if (++acc == 2) {
+      if (++acc == NACC) {
         acc = 0;
         acc_phase ^= 1u;
       }

@@ -347,6 +347,20 @@ void swiglu_mlp_inject_stall_once(int on);
  * every mode. */
 int swiglu_mlp_set_cta_pairs(int mode);
 
+/* Selects the tile width of later training calls' weight-gradient and dX
+ * GEMMs (dWd, dWgu, dX) when they run on SM pairs.  256 x 256 tiles use two
+ * TMEM accumulators, so that a tile's epilogue overlaps the next tile's
+ * main loop; 256 x 512 tiles use one accumulator of all 512 TMEM columns,
+ * each A k-block feeding twice the columns (half the B-panel reads per
+ * FLOP).  mode 1 (the default): 512 columns where the contraction is at
+ * least 16384 and every pair gets two whole tiles or more (measured 3.4%
+ * faster per training step at B=8 S=8192 D=4096 H=11008), else 256; 0: 256
+ * always; 2: 512 always.  All are deterministic and within the same
+ * tolerances (their stream-K splits differ).  A workspace sized by
+ * swiglu_mlp_workspace_bytes() fits every mode.  Returns the previous
+ * mode. */
+int swiglu_mlp_set_wide_tiles(int mode);
+
 /* Selects how later few-token no-grad calls (M <= 64, bf16/fp16) of this
  * process run: as ONE persistent kernel that hands out fixed work units (a
  * gate/up or down tile x a run of k-blocks) from a queue in the workspace,

@@ -313,6 +313,64 @@ def sample_units(H, seed):
 @pytest.mark.slow
 @pytest.mark.parametrize("dtn,B,S,D,H", SAMPLED)
 def test_full_size_sampled_parity(dtn, B, S, D, H):
+    _sampled_parity(dtn, B, S, D, H)
+
+
+@pytest.fixture
+def wide_tiles():
+    """Runs a test with 512-column pair tiles for dWd, dWgu and dX at every
+    size (the default takes them by size)."""
+    old = api.swiglu_mlp_set_wide_tiles(2)
+    yield
+    api.swiglu_mlp_set_wide_tiles(old)
+
+
+@pytest.mark.parametrize("dtn,B,S,D,H", [("bf16", 1, 8192, 1024, 4096), ("f16", 1, 8192, 1024, 4096),
+                                         ("bf16", 8, 4096, 2048, 5632)])
+def test_wide_tiles_sampled_parity(dtn, B, S, D, H, wide_tiles):
+    """512-column tiles for dWd, dWgu and dX against the oracle on the
+    sampled rows and units."""
+    _sampled_parity(dtn, B, S, D, H)
+
+
+@pytest.mark.parametrize("M,D,H", [(1000, 200, 392), (513, 648, 776), (4096, 1024, 1000)])
+def test_wide_tiles_ragged_parity(M, D, H, wide_tiles):
+    """512-column tiles with ragged edges: N not a multiple of 512 (and of
+    256), M not a multiple of 256, on SM pairs, against the full oracle."""
+    old = api.swiglu_mlp_set_cta_pairs(2)
+    try:
+        t = synthetic.make_inputs(M, D, H, "bf16", seed=M + D, device="cuda")
+        g = run_gpu(t, "bf16")
+    finally:
+        api.swiglu_mlp_set_cta_pairs(old)
+    check_all(g, run_oracle(t, "bf16"), "bf16")
+
+
+def test_wide_tiles_deterministic_and_close_to_narrow():
+    """The 512-column form gives the same bits on every call, and matches
+    the 256-column form within accumulation-order rounding (whole tiles sum
+    their k-blocks in the same order in both; stream-K-shared tiles split
+    at different points)."""
+    M, D, H = 8192, 1024, 4096
+    t = synthetic.make_inputs(M, D, H, "bf16", seed=61, device="cuda", kind="device")
+    outs = {}
+    for mode in (2, 2, 0):
+        old = api.swiglu_mlp_set_wide_tiles(mode)
+        try:
+            _, saved = api.swiglu_mlp_fwd(t["X"], t["Wgu"], t["Wd"])
+            dX, dWgu, dWd = api.swiglu_mlp_bwd(t["dY"], t["X"], t["Wgu"], t["Wd"], saved)
+            torch.cuda.synchronize()
+        finally:
+            api.swiglu_mlp_set_wide_tiles(old)
+        outs.setdefault(mode, []).append((dX.clone(), dWgu.clone(), dWd.clone()))
+    (a, b), (n,) = outs[2], outs[0]
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    for x, y in zip(a, n):
+        assert oracle.rel_frob(f64(x), f64(y)) <= 2e-3
+
+
+def _sampled_parity(dtn, B, S, D, H):
     M = B * S
     t = synthetic.make_inputs(M, D, H, dtn, seed=0, device="cuda", kind="device")
     rows = sample_rows(M, M + D)
