@@ -386,8 +386,8 @@ size_t tc_ws_part_bytes(int64_t M, int64_t D, int64_t H, int op) {
         units >= 1 ? 2 * tc_part_bytes(tc_plan(((g[0] + TC2_BM - 1) / TC2_BM) * nt, kb, units)) : 0;
     if (b1 > best) best = b1;
     if (b2 > best) best = b2;
-    if (op == SWIGLU_OP_BWD && units >= 1 && i != 1) {
-      // the same GEMM on 512-column pair tiles (dWd, dWgu, dX)
+    if (units >= 1 && (op == SWIGLU_OP_BWD ? i != 1 : i == 1)) {
+      // the same GEMM on 512-column pair tiles (dWd, dWgu, dX; the down projection)
       const int64_t ntw = (g[1] + TC2_WIDE_BN - 1) / TC2_WIDE_BN;
       const size_t bw = 2 * tc_part_bytes(tc_plan(((g[0] + TC2_BM - 1) / TC2_BM) * ntw, kb, units),
                                           TC2_WIDE_BN);
@@ -974,11 +974,16 @@ swiglu_status tc_forward(const void* X, const void* Wgu, const void* Wd, void* Y
   if (!map_kmajor(&ta, BF16, A, H, M, ld_a, TC_BM) ||
       !map_kmajor(&twd, BF16, Wd, H, D, H, pairs2 ? 128 : TC_BN))
     return SWIGLU_ERR_CUDA;
-  TcShape s2 = make_shape(M, D, H, TC_BN, err, pairs2, cap);
+  const bool wide2 = use_wide(pairs2, M, D, H);
+  TcShape s2 = make_shape(M, D, H, wide2 ? TC2_WIDE_BN : TC_BN, err, pairs2, cap);
   set_windows(s2, {{Y, (size_t)(M * D * 2)}, {err, ws_bytes}});
   EpiStore::Params p2{Y, D, o.dm, 0};
-  return cuda_status(launch_gemm<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore>(
-      pairs2, G != nullptr ? K_DOWN : K_DOWN_NOGRAD, ta, twd, s2, p2, st));
+  const int kid2 = G != nullptr ? K_DOWN : K_DOWN_NOGRAD;
+  return cuda_status(
+      wide2 ? launch_tc2<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore, TC2_WIDE_BN>(kid2, ta, twd, s2,
+                                                                              p2, st)
+            : launch_gemm<LOAD_KMAJOR, LOAD_KMAJOR, BF16, EpiStore>(pairs2, kid2, ta, twd, s2, p2,
+                                                                   st));
 }
 
 template <bool BF16>

@@ -348,7 +348,8 @@ void swiglu_mlp_inject_stall_once(int on);
 int swiglu_mlp_set_cta_pairs(int mode);
 
 /* Selects the tile width of later training calls' weight-gradient and dX
- * GEMMs (dWd, dWgu, dX) when they run on SM pairs.  256 x 256 tiles use two
+ * GEMMs (dWd, dWgu, dX) and of the down projection when they run on SM
+ * pairs.  256 x 256 tiles use two
  * TMEM accumulators, so that a tile's epilogue overlaps the next tile's
  * main loop; 256 x 512 tiles use one accumulator of all 512 TMEM columns,
  * each A k-block feeding twice the columns (half the B-panel reads per
